@@ -1,0 +1,533 @@
+#!/usr/bin/env python3
+"""Benchmark of the TurboQuant store + fused decode path on GB300.
+
+Default workload (c4): the turboquant_4bit_nc preset at head_dim 256, with
+16 query heads over 4 KV heads and 4 layers (seeds 42 + 1337 * layer).  Every
+layer's cache uses the hybrid-model page: lcm(4 * 262 B, 4096 B) = 536576 B,
+i.e. 512 tokens per block.  One step is, per layer, a bulk tq_store_kv of
+65536 new tokens followed by tq_decode_attention over 256 sequences x 2048
+cached tokens.
+
+Reported:
+  value      decode packed-KV GB/s: bytes of packed slots read by decode /
+             decode time (CUDA events on the launch stream)
+  store      tq_store_kv Mtok/s
+  e2e        the same GB/s through the public API with host buffers: per step
+             the H2D copy of new K/V, slots, queries and tables from pinned
+             memory, the step, and the D2H copy of the outputs
+  roofline   decode algorithmic bytes / time against the measured HBM peak
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
+
+``--impl reference`` times the CPU oracle itself on the same metric; its
+steps are bounded samples.  Under torchrun each rank runs its own replica on
+its own GPU ("weak" scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+METRIC = "fused TQ decode attn packed-KV HBM GB/s (% of peak); tq_store Mtok/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="c4", help="c1 | c2 | c3 | c4 (c4 is the reported configuration)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# multi-rank helpers (timing only; the data path has no collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+
+    _, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return world
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_scalar(x: float, op: str, device=None) -> float:
+    """max / sum of a per-rank scalar over all ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# accounting
+# ---------------------------------------------------------------------------
+
+def slot_bytes_cfg(head_dim: int, kb: int, vb: int) -> int:
+    key = head_dim if kb == 8 else -(-head_dim * kb // 8) + 2
+    val = -(-head_dim * vb // 8) + 4
+    s = key + val
+    return s + (s & 1)
+
+
+def decode_bytes(wl, slot_al: int):
+    """(packed-KV bytes, all algorithmic bytes) of one decode call: per
+    sequence L*H*slot packed bytes, plus q (Hq*d bf16), out (Hq*d fp32),
+    the block-table entries read and the sequence length."""
+    lens = wl.seq_lens.astype(np.int64)
+    packed = int(np.sum(lens) * wl.num_kv_heads * slot_al)
+    blocks = int(np.sum((lens + wl.block_size - 1) // wl.block_size))
+    other = wl.num_seqs * (wl.num_q_heads * wl.head_dim * (2 + 4) + 4) + 4 * blocks
+    return packed, packed + other
+
+
+def store_bytes_per_token(wl, slot_al: int) -> int:
+    """bf16 K and V read, the packed token row written, the int64 slot id."""
+    return 2 * wl.num_kv_heads * wl.head_dim * 2 + wl.num_kv_heads * slot_al + 8
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return float(d["hbm_gbs"]), "measured"
+        except (KeyError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_traffic_record():
+    """DRAM bytes per decode launch from the committed ncu summary, used only
+    while the decode source is unchanged since the capture (else None)."""
+    f = ROOT / "profiles" / "decode_traffic.txt"
+    if not f.exists():
+        return None
+    vals = {}
+    for line in f.read_text().splitlines():
+        if "=" in line and not line.lstrip().startswith("#"):
+            key, val = line.split("=", 1)
+            vals[key.strip()] = val.strip()
+    src = ROOT / "kv_cache_quantization_store_gb300" / "csrc" / "tq_decode.cu"
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    if vals.get("source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_c4"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        for line in Path(self.file.name).read_text().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import kv_cache_quantization_store_gb300 as tq
+    from kv_cache_quantization_store_gb300 import build as tq_build
+    from kv_cache_quantization_store_gb300 import workloads as W
+
+    rank, world, local_rank = dist_env()
+    dist_init("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0:
+        tq_build.build()
+    barrier()
+    wl = W.named(args.workload)
+    cfg = tq.tq_config_init(wl.head_dim, wl.key_bits, wl.value_bits, wl.norm_correction, wl.seed)
+    slot_al = cfg.slot_size_aligned
+    table_np, nblk = wl.layout()
+    sm_np = wl.slot_mapping()
+    n_tok = wl.num_tokens
+    store_n = wl.store_tokens or n_tok
+    layers = list(wl.layers)
+    h, d = wl.num_kv_heads, wl.head_dim
+
+    # ---- inputs resident in HBM ------------------------------------------------
+    k_all = torch.empty((n_tok, h, d), dtype=torch.bfloat16, device=dev)
+    v_all = torch.empty_like(k_all)
+    piece = 65536
+    for a in range(0, n_tok, piece):
+        kc, vc = wl.kv(a, min(n_tok, a + piece))
+        k_all[a:a + kc.shape[0]].copy_(torch.from_numpy(kc).to(torch.bfloat16))
+        v_all[a:a + vc.shape[0]].copy_(torch.from_numpy(vc).to(torch.bfloat16))
+    slots_all = torch.from_numpy(sm_np).to(dev)
+    q = torch.from_numpy(wl.q()).to(torch.bfloat16).to(dev)
+    table = torch.from_numpy(table_np).to(dev)
+    lens = torch.from_numpy(wl.seq_lens.astype(np.int32)).to(dev)
+    max_len = int(wl.seq_lens.max())
+    caches = [tq.new_paged_cache(cfg, nblk, wl.block_size, h, l, block_stride=wl.block_stride, device=dev)
+              for l in layers]
+    for c in caches:  # prefill every layer's history (untimed)
+        tq.tq_store_kv(cfg, k_all, v_all, slots_all, c)
+    k_new, v_new, slots_new = k_all[:store_n], v_all[:store_n], slots_all[:store_n]
+    ws_bytes = tq.tq_decode_workspace_size(cfg, wl.num_seqs, wl.num_q_heads, h, wl.block_size, max_len)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    outs = [torch.empty((wl.num_seqs, wl.num_q_heads, d), dtype=torch.float32, device=dev) for _ in layers]
+    torch.cuda.synchronize()
+    for c in caches:
+        if c.error_flags():
+            raise RuntimeError(f"cache error flags {c.error_flags()} after prefill")
+
+    stream = torch.cuda.current_stream()
+    n_ev = max(1, args.steps) * len(layers)
+    ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for k in ("s0", "s1", "d0", "d1")}
+
+    def step(i=None):
+        for j, (c, o) in enumerate(zip(caches, outs)):
+            if i is not None:
+                ev["s0"][i * len(layers) + j].record(stream)
+            tq.tq_store_kv(cfg, k_new, v_new, slots_new, c, stream=stream)
+            if i is not None:
+                ev["s1"][i * len(layers) + j].record(stream)
+                ev["d0"][i * len(layers) + j].record(stream)
+            tq.tq_decode_attention(cfg, q, c, table, lens, max_len, o, ws, stream=stream)
+            if i is not None:
+                ev["d1"][i * len(layers) + j].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(torch.cuda.current_device())
+    with ClockSampler(gpu_id) as clocks:
+        torch.cuda.synchronize()
+        barrier()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = t0.elapsed_time(t1)
+    store_ms = sum(a.elapsed_time(b) for a, b in zip(ev["s0"], ev["s1"]))
+    dec_ms = sum(a.elapsed_time(b) for a, b in zip(ev["d0"], ev["d1"]))
+    for c in caches:
+        if c.error_flags():
+            raise RuntimeError(f"cache error flags {c.error_flags()} after the timed steps")
+
+    packed, algo = decode_bytes(wl, slot_al)
+    n_calls = args.steps * len(layers)
+    dec_ms_max = reduce_scalar(dec_ms, "max", dev)
+    store_ms_max = reduce_scalar(store_ms, "max", dev)
+    total_ms_max = reduce_scalar(total_ms, "max", dev)
+    value = world * packed * n_calls / (dec_ms_max * 1e-3) / 1e9
+    store_mtok = world * store_n * n_calls / (store_ms_max * 1e-3) / 1e6
+    peak, peak_kind = measured_peaks()
+    dec_avg_s = dec_ms / n_calls * 1e-3
+    achieved = algo / dec_avg_s / 1e9
+    store_gbs = store_bytes_per_token(wl, slot_al) * store_n / (store_ms / n_calls * 1e-3) / 1e9
+
+    # ---- end to end through host buffers ---------------------------------------
+    e2e = run_e2e(args, tq, wl, cfg, caches, k_new, v_new, slots_new, q, table, lens, max_len, ws, outs, stream,
+                  packed, dev)
+
+    clk = clocks.summary()
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms_max / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": workload_config(wl, cfg, slot_al, world),
+        "store": {"value": round(store_mtok, 2), "unit": "Mtok/s", "tokens_per_call": store_n,
+                  "hbm_gbs": round(store_gbs, 1), "frac": round(store_gbs / peak, 4),
+                  "peak_kind": f"{peak_kind} copy bandwidth"},
+        "decode_frac_of_peak": round(packed / dec_avg_s / 1e9 / peak, 4),
+        "roofline": {"kernel": "tq_decode_attention", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": peak_kind, "traffic": decode_traffic_record(),
+                     "algorithmic_bytes_per_launch": algo, "avg_launch_us": round(dec_avg_s * 1e6, 2)},
+        "e2e": e2e,
+        "gpu_launches": n_calls * 3,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        result["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(args, tq, wl, cfg, caches, k_new, v_new, slots_new, q, table, lens, max_len, ws, outs, stream,
+            packed, dev):
+    import torch
+
+    host = {name: t.cpu().pin_memory() for name, t in
+            (("k", k_new), ("v", v_new), ("slots", slots_new), ("q", q), ("table", table), ("lens", lens))}
+    dev_in = {name: torch.empty_like(t, device=dev) for name, t in host.items()}
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for name, t in host.items():
+            dev_in[name].copy_(t, non_blocking=True)
+        for c, o in zip(caches, outs):
+            tq.tq_store_kv(cfg, dev_in["k"], dev_in["v"], dev_in["slots"], c, stream=stream)
+            tq.tq_decode_attention(cfg, dev_in["q"], c, dev_in["table"], dev_in["lens"], max_len, o, ws,
+                                   stream=stream)
+        for o, ho in zip(outs, host_out):
+            ho.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_scalar(a.elapsed_time(b), "max", dev)
+    _, world, _ = dist_env()
+    value = world * packed * len(caches) * args.e2e_steps / (ms * 1e-3) / 1e9
+    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": args.e2e_steps, "ms_per_step": round(ms / args.e2e_steps, 4),
+            "api": "kv_cache_quantization_store_gb300.tq_store_kv / tq_decode_attention (C ABI via ctypes)"}
+
+
+def workload_config(wl, cfg, slot_al, world):
+    page = wl.block_stride or wl.block_size * wl.num_kv_heads * slot_al
+    return {
+        "workload": f"{wl.name}: {wl.description}",
+        "preset": wl.preset,
+        "head_dim": wl.head_dim,
+        "key_bits": wl.key_bits,
+        "value_bits": wl.value_bits,
+        "norm_correction": bool(wl.norm_correction),
+        "num_q_heads": wl.num_q_heads,
+        "num_kv_heads": wl.num_kv_heads,
+        "layers": len(wl.layers),
+        "decode_batch": wl.num_seqs,
+        "seq_len": int(wl.seq_lens.max()) if len(set(wl.seq_lens.tolist())) == 1 else "ragged",
+        "store_tokens": wl.store_tokens or wl.num_tokens,
+        "block_size": wl.block_size,
+        "block_bytes": page,
+        "slot_bytes": slot_al,
+        "cache_bytes_per_layer": page * wl.layout()[1],
+        "l2": "no flush: each layer's decode reads its own >129 MB cache and the store reads >129 MB of K/V",
+        "parallelism": f"replicas x{world}",
+        "kv": "one K/V draw shared by the layers; layers differ by seed (random signs)",
+    }
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl_name: str, budget_s: float, layer_idx: int = 0, max_seqs: int | None = None):
+    """Times the oracle on whole sequences of the workload until the budget is
+    spent: its store of each sequence's tokens, then its decode of them."""
+    import oracle as O
+    from kv_cache_quantization_store_gb300 import workloads as W
+
+    wl = W.named(wl_name)
+    ocfg = O.Config(head_dim=wl.head_dim, key_quant_bits=wl.key_bits, value_quant_bits=wl.value_bits,
+                    seed=wl.seed, norm_correction=wl.norm_correction)
+    layer = O.make_layer(ocfg, layer_idx)
+    table, nblk = wl.layout()
+    cache = O.new_cache(ocfg, nblk, wl.block_size, wl.num_kv_heads, wl.block_stride)
+    q_all = wl.q()
+    cu = wl.cu_seqlens()
+    sm = wl.slot_mapping()
+    t_store = t_dec = 0.0
+    toks = packed = 0
+    seqs = 0
+    per_seq = []
+    start = time.perf_counter()
+    for s in range(wl.num_seqs):
+        a, b = int(cu[s]), int(cu[s + 1])
+        k, v = wl.kv(a, b, threads=1)
+        t = time.perf_counter()
+        O.store_kv(layer, k, v, sm[a:b], cache)
+        ts = time.perf_counter() - t
+        t = time.perf_counter()
+        O.decode_attention(layer, q_all[s:s + 1], cache, table[s:s + 1], wl.seq_lens[s:s + 1])
+        td = time.perf_counter() - t
+        t_store += ts
+        t_dec += td
+        per_seq.append((b - a, ts, td))
+        toks += b - a
+        packed += (b - a) * wl.num_kv_heads * ocfg.slot_size_aligned
+        seqs += 1
+        if time.perf_counter() - start > budget_s or (max_seqs and seqs >= max_seqs):
+            break
+    return {"decode_gbs": packed / t_dec / 1e9, "store_mtok_s": toks / t_store / 1e6, "seqs": seqs,
+            "tokens": toks, "decode_s": t_dec, "store_s": t_store, "per_seq": per_seq,
+            "slot_bytes": ocfg.slot_size_aligned, "num_kv_heads": wl.num_kv_heads}
+
+
+def oracle_child_env():
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    return env
+
+
+def run_oracle_child(wl_name: str, budget: float, max_seqs: int | None = None):
+    cmd = [sys.executable, str(Path(__file__).resolve()), "--oracle-child",
+           json.dumps({"workload": wl_name, "budget": budget, "max_seqs": max_seqs})]
+    res = subprocess.run(cmd, env=oracle_child_env(), capture_output=True, text=True, timeout=1800)
+    if res.returncode != 0:
+        raise RuntimeError(f"oracle child failed: {res.stderr[-2000:]}")
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(args):
+    r = run_oracle_child(args.workload, args.cpu_seconds)
+    return {"value": round(r["decode_gbs"], 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{r['seqs']} whole sequences of {args.workload} (layer 0): oracle store of their "
+                       f"{r['tokens']} tokens then oracle decode of all query heads; single thread "
+                       "(BLAS pinned to 1)"),
+            "store_mtok_s": round(r["store_mtok_s"], 6), "host_cores_available": len(os.sched_getaffinity(0))}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: one step = one whole sequence of
+    the workload (layer 0): the oracle's store of its tokens, then its decode
+    of every query head.  Rank 0 alone runs; other ranks exit."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    r = run_oracle_child(args.workload, float("inf"), max_seqs=args.warmup + args.steps)
+    timed = r["per_seq"][args.warmup:]
+    if not timed:
+        raise RuntimeError("no timed reference steps")
+    dec_s = sum(td for _, _, td in timed)
+    store_s = sum(ts for _, ts, _ in timed)
+    toks = sum(n for n, _, _ in timed)
+    value = toks * r["num_kv_heads"] * r["slot_bytes"] / dec_s / 1e9
+    sample = (f"each step: one whole sequence of {args.workload} (layer 0, {timed[0][0]} tokens): "
+              "oracle store then oracle decode of every query head, single thread (BLAS pinned to 1)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
+        "steps": len(timed), "warmup": args.warmup, "ms_per_step": round((dec_s + store_s) / len(timed) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "impl": "CPU oracle (NumPy fp64)"},
+        "store": {"value": round(toks / store_s / 1e6, 6), "unit": "Mtok/s"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "kind": "oracle", "cores": 1, "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.oracle_child:
+        spec = json.loads(args.oracle_child)
+        sys.path.insert(0, str(ROOT))
+        budget = spec["budget"] if spec["budget"] is not None else float("inf")
+        r = oracle_sample(spec["workload"], budget, max_seqs=spec.get("max_seqs"))
+        print(json.dumps(r))
+        return
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,412 @@
+// Fused decode attention over the packed cache, split-KV.
+//
+// [ART] hnwysp.cn TurboQuant article, "Direction 1": score the rotated query
+// against the compressed keys (q . k_hat = vec_norm * (Pi q) . c~), run an
+// online softmax block by block, never expand K or V.  [TQC] norm_correction
+// divides by ||c~|| (the centroid vector's norm).
+//
+// Grid: (split, sequence).  A CTA walks its range of 16-token chunks; each
+// chunk is the contiguous span of 16 token rows (all KV heads) inside one
+// paged block, staged into shared memory with 16-byte cp.async copies
+// (double-buffered).  Per chunk:
+//   1. scores: (token, head) items, a few threads each, dot the rotated,
+//      pre-scaled queries with the looked-up centroids (or FP8 keys);
+//   2. online-softmax update per query head (max, rescale, probabilities);
+//   3. P.V: warp h owns KV head h, each lane d/32 dims of all its queries.
+// Each CTA writes a partial (m, l, o) per query head; a second kernel merges
+// the splits by log-sum-exp.
+#include <cmath>
+
+#include "tq_device.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTokPerChunk = 16;
+constexpr int kMaxG = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+struct DecodeArgs {
+    const uint16_t* q;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    float* partials;  // [S, Hq, splits, D + 2]
+    int num_q_heads;
+    int max_blocks;
+    int max_seq_len;
+    int chunks_per_split;
+    int num_splits;
+    float qscale;  // sm_scale * log2(e)
+};
+
+__host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
+
+// Shared-memory layout (bytes), all offsets 16-byte aligned.
+struct SmemLayout {
+    int q_off, sc_off, st_off, buf_off, buf_bytes, total;
+    __host__ __device__ SmemLayout(int hq, int d, int h, int slot_al) {
+        q_off = 0;
+        sc_off = align16(q_off + hq * d * 4);
+        st_off = align16(sc_off + hq * kTokPerChunk * 4);
+        buf_off = align16(st_off + (3 * hq + 16) * 4);
+        buf_bytes = kTokPerChunk * h * slot_al;
+        total = buf_off + 2 * buf_bytes;
+    }
+};
+
+template <int D, int KB, int VB>
+__global__ void __launch_bounds__(kThreads)
+decode_kernel(const LayerParams p, const CacheGeom c, const DecodeArgs a) {
+    using S = Slot<D, KB, VB>;
+    constexpr int SA = S::kAligned;
+    constexpr int DPT = D >= 32 ? D / 32 : 1;  // P.V dims per lane
+    extern __shared__ __align__(16) uint8_t smem[];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int split = blockIdx.x;
+    const int s = blockIdx.y;
+    const int H = c.num_kv_heads;
+    const int Hq = a.num_q_heads;
+    const int G = Hq / H;
+    const SmemLayout lay(Hq, D, H, SA);
+    float* qs = reinterpret_cast<float*>(smem + lay.q_off);   // [Hq][D] rotated, scaled queries
+    float* sc = reinterpret_cast<float*>(smem + lay.sc_off);  // [Hq][16] scores -> probabilities
+    float* m_s = reinterpret_cast<float*>(smem + lay.st_off); // [Hq]
+    float* l_s = m_s + Hq;
+    float* al_s = l_s + Hq;
+    float* ctab = al_s + Hq;                                  // [16] centroids
+    uint8_t* bufs = smem + lay.buf_off;
+
+    // ---- sequence range ----------------------------------------------------
+    int L = a.seq_lens[s];
+    const int cap = min(a.max_seq_len, a.max_blocks * c.block_size);
+    if (L > cap || L < 0) {
+        if (tid == 0 && split == 0) set_flag(c.flags, kFlagSeq);
+        L = L < 0 ? 0 : cap;
+    }
+    const int n_chunks = (L + kTokPerChunk - 1) / kTokPerChunk;
+    const int c0 = split * a.chunks_per_split;
+    const int c1 = min(c0 + a.chunks_per_split, n_chunks);
+
+    // ---- prologue: queries -> Pi q (MSE keys) scaled for exp2 ---------------
+    const uint16_t* qg = a.q + static_cast<int64_t>(s) * Hq * D;
+    for (int i = tid; i < Hq * D; i += kThreads) {
+        float x = __uint_as_float(static_cast<uint32_t>(qg[i]) << 16);
+        if constexpr (KB != 8) {
+            const int dim = i % D;
+            if ((p.sign_mask[dim >> 5] >> (dim & 31)) & 1u) x = -x;
+        }
+        qs[i] = x;
+    }
+    if constexpr (KB != 8) {
+#pragma unroll 1
+        for (int st = 1; st < D; st <<= 1) {
+            __syncthreads();
+            for (int b = tid; b < Hq * D / 2; b += kThreads) {
+                const int row = b / (D / 2);
+                const int j = b % (D / 2);
+                const int i = (j / st) * 2 * st + (j % st);
+                float* r = qs + row * D;
+                const float x0 = r[i], x1 = r[i + st];
+                r[i] = x0 + x1;
+                r[i + st] = x0 - x1;
+            }
+        }
+    }
+    __syncthreads();
+    {
+        const float f = (KB != 8) ? a.qscale * rsqrtf(static_cast<float>(D)) : a.qscale;
+        for (int i = tid; i < Hq * D; i += kThreads) qs[i] *= f;
+    }
+    if (tid < Hq) {
+        m_s[tid] = -INFINITY;
+        l_s[tid] = 0.f;
+        al_s[tid] = 1.f;
+    }
+    if (tid < 16) ctab[tid] = tid < p.n_centroids ? p.centroids[tid] : 0.f;
+
+    // ---- chunk staging ------------------------------------------------------
+    auto chunk_block = [&](int ci) -> int {
+        const int b = a.block_table[static_cast<int64_t>(s) * a.max_blocks + (ci * kTokPerChunk) / c.block_size];
+        return (b >= 0 && b < c.num_blocks) ? b : -1;
+    };
+    auto stage = [&](int ci, uint8_t* dst) {
+        const int b = chunk_block(ci);
+        if (b < 0) return;
+        const uint8_t* src = c.data + static_cast<int64_t>(b) * c.block_stride +
+                             static_cast<int64_t>((ci * kTokPerChunk) % c.block_size) * H * SA;
+        const int pieces = lay.buf_bytes / 16;
+        for (int i = tid; i < pieces; i += kThreads) cp_async16(dst + 16 * i, src + 16 * i);
+    };
+
+    // P.V accumulators: warp h = KV head h, lane owns dims [lane*DPT, +DPT).
+    float o[kMaxG][DPT];
+#pragma unroll
+    for (int g = 0; g < kMaxG; ++g)
+#pragma unroll
+        for (int k = 0; k < DPT; ++k) o[g][k] = 0.f;
+
+    // Score work split: 16*H (token, head) items, tpi threads each.  When
+    // tpi > 1, items * tpi is a multiple of 32, so the shuffles below run in
+    // whole warps.
+    const int items = kTokPerChunk * H;
+    int tpi = 1;
+    while (tpi * 2 * items <= kThreads && tpi * 2 <= 32 && tpi * 2 <= D) tpi *= 2;
+    const int item = tid / tpi;
+    const int sub = tid % tpi;
+    const int dpt = D / tpi;
+
+    if (c0 < c1) stage(c0, bufs);
+    cp_async_commit();
+#pragma unroll 1
+    for (int ci = c0; ci < c1; ++ci) {
+        uint8_t* cur = bufs + ((ci - c0) & 1) * lay.buf_bytes;
+        if (ci + 1 < c1) stage(ci + 1, bufs + ((ci + 1 - c0) & 1) * lay.buf_bytes);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const bool chunk_ok = chunk_block(ci) >= 0;
+        if (!chunk_ok && tid == 0) set_flag(c.flags, kFlagBlock);
+        const int tok0 = ci * kTokPerChunk;
+
+        // 1. scores
+        if (item < items) {
+            const int t = item % kTokPerChunk;
+            const int h = item / kTokPerChunk;
+            const uint8_t* slot = cur + (t * H + h) * SA;
+            float acc[kMaxG];
+#pragma unroll
+            for (int g = 0; g < kMaxG; ++g) acc[g] = 0.f;
+            float nsq = 0.f;
+            const float* qrow = qs + h * G * D;
+#pragma unroll 4
+            for (int i = sub * dpt; i < (sub + 1) * dpt; ++i) {
+                float cv;
+                if constexpr (KB == 8) {
+                    cv = e4m3_to_float(slot[i]);
+                } else {
+                    const int bit = i * KB;
+                    const uint32_t win = static_cast<uint32_t>(slot[bit >> 3]) |
+                                         (static_cast<uint32_t>(slot[(bit >> 3) + 1]) << 8);
+                    cv = ctab[(win >> (bit & 7)) & ((1u << KB) - 1u)];
+                    nsq = fmaf(cv, cv, nsq);
+                }
+#pragma unroll
+                for (int g = 0; g < kMaxG; ++g)
+                    if (g < G) acc[g] = fmaf(qrow[g * D + i], cv, acc[g]);
+            }
+            for (int m = 1; m < tpi; m <<= 1) {
+#pragma unroll
+                for (int g = 0; g < kMaxG; ++g) acc[g] += __shfl_xor_sync(kFull, acc[g], m);
+                nsq += __shfl_xor_sync(kFull, nsq, m);
+            }
+            if (sub == 0) {
+                const bool ok = chunk_ok && (tok0 + t < L);
+                float f = 1.f;
+                if constexpr (KB != 8) {
+                    f = half_from_bits(*reinterpret_cast<const uint16_t*>(slot + S::kKeyIdxBytes));
+                    if (p.nc) f = f / sqrtf(nsq);
+                }
+#pragma unroll
+                for (int g = 0; g < kMaxG; ++g)
+                    if (g < G) sc[(h * G + g) * kTokPerChunk + t] = ok ? acc[g] * f : -INFINITY;
+            }
+        }
+        __syncthreads();
+
+        // 2. online softmax state per query head
+        if (tid < Hq) {
+            float* row = sc + tid * kTokPerChunk;
+            const float m_old = m_s[tid];
+            float mx = m_old;
+#pragma unroll
+            for (int t = 0; t < kTokPerChunk; ++t) mx = fmaxf(mx, row[t]);
+            const float alpha = (mx == -INFINITY) ? 1.f : exp2f(m_old - mx);
+            float sum = 0.f;
+#pragma unroll
+            for (int t = 0; t < kTokPerChunk; ++t) {
+                const float pr = (row[t] == -INFINITY) ? 0.f : exp2f(row[t] - mx);
+                row[t] = pr;
+                sum += pr;
+            }
+            l_s[tid] = l_s[tid] * alpha + sum;
+            m_s[tid] = mx;
+            al_s[tid] = alpha;
+        }
+        __syncthreads();
+
+        // 3. P.V
+        if (warp < H && (D >= 32 || lane < D)) {
+            const int h = warp;
+#pragma unroll
+            for (int g = 0; g < kMaxG; ++g) {
+                if (g < G) {
+                    const float al = al_s[h * G + g];
+#pragma unroll
+                    for (int k = 0; k < DPT; ++k) o[g][k] *= al;
+                }
+            }
+            const int ntok = chunk_ok ? min(kTokPerChunk, L - tok0) : 0;
+            for (int t = 0; t < ntok; ++t) {
+                const uint8_t* slot = cur + (t * H + h) * SA;
+                const uint16_t* sz = reinterpret_cast<const uint16_t*>(slot + S::kKeyBytes + S::kValCodeBytes);
+                const float vs = half_from_bits(sz[0]);
+                const float vz = half_from_bits(sz[1]);
+                const uint8_t* codes = slot + S::kKeyBytes;
+                float val[DPT];
+#pragma unroll
+                for (int k = 0; k < DPT; ++k) {
+                    const int i = lane * DPT + k;
+                    const int bit = i * VB;
+                    const uint32_t win = static_cast<uint32_t>(codes[bit >> 3]) |
+                                         (static_cast<uint32_t>(codes[(bit >> 3) + 1]) << 8);
+                    val[k] = fmaf(vs, static_cast<float>((win >> (bit & 7)) & ((1u << VB) - 1u)), vz);
+                }
+#pragma unroll
+                for (int g = 0; g < kMaxG; ++g) {
+                    if (g < G) {
+                        const float pr = sc[(h * G + g) * kTokPerChunk + t];
+#pragma unroll
+                        for (int k = 0; k < DPT; ++k) o[g][k] = fmaf(pr, val[k], o[g][k]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+
+    // ---- partial state -------------------------------------------------------
+    if (warp < H && (D >= 32 || lane < D)) {
+        const int h = warp;
+#pragma unroll
+        for (int g = 0; g < kMaxG; ++g) {
+            if (g < G) {
+                const int hq = h * G + g;
+                float* part = a.partials + ((static_cast<int64_t>(s) * Hq + hq) * a.num_splits + split) * (D + 2);
+                if (lane == 0) {
+                    part[0] = m_s[hq];
+                    part[1] = l_s[hq];
+                }
+#pragma unroll
+                for (int k = 0; k < DPT; ++k) part[2 + lane * DPT + k] = o[g][k];
+            }
+        }
+    }
+}
+
+// Log-sum-exp merge of the split partials: one CTA per (query head, sequence),
+// one thread per output dimension.
+__global__ void combine_kernel(const float* __restrict__ partials, float* __restrict__ out, int Hq, int D,
+                               int num_splits) {
+    const int hq = blockIdx.x, s = blockIdx.y;
+    const float* base = partials + (static_cast<int64_t>(s) * Hq + hq) * num_splits * (D + 2);
+    float M = -INFINITY;
+    for (int sp = 0; sp < num_splits; ++sp) M = fmaxf(M, base[sp * (D + 2)]);
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        float lsum = 0.f, acc = 0.f;
+        if (M != -INFINITY) {
+            for (int sp = 0; sp < num_splits; ++sp) {
+                const float m = base[sp * (D + 2)];
+                if (m == -INFINITY) continue;
+                const float w = exp2f(m - M);
+                lsum = fmaf(base[sp * (D + 2) + 1], w, lsum);
+                acc = fmaf(base[sp * (D + 2) + 2 + i], w, acc);
+            }
+        }
+        out[(static_cast<int64_t>(s) * Hq + hq) * D + i] = lsum > 0.f ? acc / lsum : 0.f;
+    }
+}
+
+template <int D, int KB, int VB>
+cudaError_t launch(const LayerParams& p, const CacheGeom& c, const DecodeArgs& a, int num_seqs, float* out,
+                   cudaStream_t stream) {
+    const SmemLayout lay(a.num_q_heads, D, c.num_kv_heads, Slot<D, KB, VB>::kAligned);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         lay.total);
+    if (e != cudaSuccess) return e;
+    dim3 grid(static_cast<unsigned>(a.num_splits), static_cast<unsigned>(num_seqs));
+    decode_kernel<D, KB, VB><<<grid, kThreads, lay.total, stream>>>(p, c, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 cgrid(static_cast<unsigned>(a.num_q_heads), static_cast<unsigned>(num_seqs));
+    combine_kernel<<<cgrid, D < 128 ? 128 : D, 0, stream>>>(a.partials, out, a.num_q_heads, D, a.num_splits);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const DecodeArgs& a, int ns, float* out,
+                          cudaStream_t st) {
+    const int kb = p.kbits, vb = p.vbits;
+    if (kb == 3 && vb == 3) return launch<D, 3, 3>(p, c, a, ns, out, st);
+    if (kb == 3 && vb == 4) return launch<D, 3, 4>(p, c, a, ns, out, st);
+    if (kb == 4 && vb == 3) return launch<D, 4, 3>(p, c, a, ns, out, st);
+    if (kb == 4 && vb == 4) return launch<D, 4, 4>(p, c, a, ns, out, st);
+    if (kb == 8 && vb == 3) return launch<D, 8, 3>(p, c, a, ns, out, st);
+    if (kb == 8 && vb == 4) return launch<D, 8, 4>(p, c, a, ns, out, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+DecodePlan plan_decode(const LayerParams& p, int num_seqs, int num_q_heads, int num_kv_heads, int max_seq_len,
+                       int num_splits_req, int sm_count) {
+    (void)num_kv_heads;
+    DecodePlan plan{};
+    const int max_chunks = (max_seq_len + kTokPerChunk - 1) / kTokPerChunk;
+    int splits;
+    if (num_splits_req > 0) {
+        splits = num_splits_req;
+    } else {
+        const int target = 2 * (sm_count > 0 ? sm_count : 1);
+        splits = num_seqs > 0 ? (target + num_seqs - 1) / num_seqs : 1;
+    }
+    if (splits > max_chunks) splits = max_chunks;
+    if (splits < 1) splits = 1;
+    int cps = max_chunks > 0 ? (max_chunks + splits - 1) / splits : 0;
+    if (cps > 0) splits = (max_chunks + cps - 1) / cps;
+    plan.num_splits = splits;
+    plan.chunks_per_split = cps;
+    plan.partial_bytes = static_cast<size_t>(num_seqs) * num_q_heads * splits * (p.d + 2) * sizeof(float);
+    plan.workspace_bytes = (plan.partial_bytes + 255) & ~static_cast<size_t>(255);
+    if (plan.workspace_bytes == 0) plan.workspace_bytes = 256;
+    return plan;
+}
+
+cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16_t* q, int num_seqs,
+                          int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens, int max_seq_len, float sm_scale, const DecodePlan& plan,
+                          float* out, void* workspace, cudaStream_t stream) {
+    DecodeArgs a{};
+    a.q = q;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.partials = static_cast<float*>(workspace);
+    a.num_q_heads = num_q_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.max_seq_len = max_seq_len;
+    a.chunks_per_split = plan.chunks_per_split;
+    a.num_splits = plan.num_splits;
+    a.qscale = sm_scale * kLog2e;
+    switch (p.d) {
+        case 16: return dispatch_bits<16>(p, c, a, num_seqs, out, stream);
+        case 32: return dispatch_bits<32>(p, c, a, num_seqs, out, stream);
+        case 64: return dispatch_bits<64>(p, c, a, num_seqs, out, stream);
+        case 128: return dispatch_bits<128>(p, c, a, num_seqs, out, stream);
+        case 256: return dispatch_bits<256>(p, c, a, num_seqs, out, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace tq

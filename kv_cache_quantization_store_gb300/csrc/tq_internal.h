@@ -1,0 +1,72 @@
+// Internal interface between the host core (tq_host.cpp) and the CUDA
+// kernels.  Nothing here is part of the public ABI (include/tq.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace tq {
+
+// Everything a kernel needs to know about one layer's quantiser; passed by
+// value as a kernel parameter (under 300 bytes).
+struct LayerParams {
+    int32_t d;
+    int32_t kbits;
+    int32_t vbits;
+    int32_t nc;
+    int32_t key_fp8;
+    int32_t mse_bits;
+    int32_t n_centroids;
+    int32_t key_packed;
+    int32_t value_packed;
+    int32_t slot_al;
+    uint32_t sign_mask[8];  // bit i set: s_i = -1 (d <= 256)
+    float centroids[16];
+    float boundaries[15];
+};
+
+struct CacheGeom {
+    uint8_t* data;
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int64_t block_stride;  // bytes, > 0
+    uint32_t* flags;       // may be null
+};
+
+constexpr uint32_t kFlagSlot = 1u;
+constexpr uint32_t kFlagBlock = 2u;
+constexpr uint32_t kFlagSeq = 4u;
+
+struct DecodePlan {
+    int32_t num_splits;
+    int32_t chunks_per_split;  // 16-token chunks handled by one split
+    size_t partial_bytes;      // fp32 partial states
+    size_t workspace_bytes;    // total, including alignment padding
+};
+
+// Chooses the split count for a decode call (num_splits_req = 0: automatic).
+DecodePlan plan_decode(const LayerParams& p, int num_seqs, int num_q_heads, int num_kv_heads,
+                       int max_seq_len, int num_splits_req, int sm_count);
+
+cudaError_t launch_store(const LayerParams& p, const CacheGeom& c, const uint16_t* k,
+                         const uint16_t* v, int64_t num_tokens, const int64_t* slot_mapping,
+                         int sm_count, cudaStream_t stream);
+
+cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16_t* q, int num_seqs,
+                          int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens, int max_seq_len, float sm_scale,
+                          const DecodePlan& plan, float* out, void* workspace, cudaStream_t stream);
+
+cudaError_t launch_dequant(const LayerParams& p, const CacheGeom& c, const int32_t* block_table,
+                           int max_blocks_per_seq, const int32_t* cu_seqlens, int num_seqs,
+                           int max_seq_len, uint16_t* k_out, uint16_t* v_out, cudaStream_t stream);
+
+// Supported compile-time shapes.
+inline bool supported_head_dim(int d) {
+    return d == 16 || d == 32 || d == 64 || d == 128 || d == 256;
+}
+
+}  // namespace tq

@@ -1,0 +1,218 @@
+// Store path: quantise new keys/values and scatter their packed slots into
+// the paged cache.
+//
+// [TQC] TurboQuantConfig (vLLM API docs, quantization.turboquant): slot layout
+// [key_packed | value_packed]; key_packed = MSE indices + fp16 vec_norm, or d
+// FP8 bytes; value_packed = codes + fp16 scale + fp16 zero.  Key transform:
+// random-sign Walsh-Hadamard rotation then Lloyd-Max scalar quantisation.
+//
+// Work decomposition: one (token, KV head) vector is split into LPV lane
+// parts of EPL = min(d, 32) consecutive elements, so one warp handles
+// 32 / LPV consecutive vectors per iteration (a whole token row when
+// H * d = 1024).  The rotation is an in-register FWHT over the lane's EPL
+// elements followed by log2(LPV) shuffle stages.  Each warp assembles its
+// slots in shared memory and copies them to the cache with 2-byte stores,
+// because a slot is only 2-byte aligned.
+#include "tq_device.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kStoreWarps = 8;
+
+template <int D, int KB, int VB>
+__global__ void __launch_bounds__(kStoreWarps * 32)
+store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict__ k,
+             const uint16_t* __restrict__ v, const int64_t num_tokens,
+             const int64_t* __restrict__ slot_mapping) {
+    using S = Slot<D, KB, VB>;
+    using LS = LaneSplit<D>;
+    constexpr int EPL = LS::kEPL, LPV = LS::kLPV, VPW = LS::kVPW;
+    constexpr int SA = S::kAligned;
+    constexpr int kTopV = (1 << VB) - 1;
+    constexpr int kHalf = KB == 8 ? 2 : (1 << KB) / 2;  // levels per sign
+
+    __shared__ __align__(16) uint8_t stage_all[kStoreWarps][VPW * SA + 2];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    uint8_t* stage = stage_all[warp];
+    const int part = lane % LPV;
+    const int vin = lane / LPV;
+    const int H = c.num_kv_heads;
+    const int64_t num_vecs = num_tokens * H;
+
+    // This lane's slice of the sign diagonal, and the positive-half decision
+    // thresholds (the grid is symmetric about 0 and the middle boundary is 0).
+    uint32_t signs = 0;
+    float pos_b[kHalf - 1];
+    if constexpr (KB != 8) {
+        const int first = part * EPL;
+        signs = p.sign_mask[first / 32] >> (first % 32);
+#pragma unroll
+        for (int j = 0; j < kHalf - 1; ++j) pos_b[j] = p.boundaries[kHalf + j];
+    }
+    const float sqrt_d = sqrtf(static_cast<float>(D));
+
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kStoreWarps * VPW;
+    for (int64_t base = (static_cast<int64_t>(blockIdx.x) * kStoreWarps + warp) * VPW; base < num_vecs;
+         base += step) {
+        const int64_t vi = base + vin;
+        const bool valid = vi < num_vecs;
+        const int64_t vsafe = valid ? vi : num_vecs - 1;
+        uint8_t* my_slot = stage + vin * SA;
+
+        // ---- key -----------------------------------------------------------
+        {
+            float x[EPL];
+            load_bf16<EPL>(k + vsafe * D + part * EPL, x);
+            if constexpr (KB == 8) {
+                // FP8 e4m3, round to nearest even, saturating finite.
+                uint32_t w[EPL / 4];
+#pragma unroll
+                for (int j = 0; j < EPL / 4; ++j) {
+                    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * j], x[4 * j + 1]),
+                                                                 __NV_SATFINITE, __NV_E4M3);
+                    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * j + 2], x[4 * j + 3]),
+                                                                 __NV_SATFINITE, __NV_E4M3);
+                    w[j] = (lo & 0xffffu) | (hi << 16);
+                }
+                write_u16_words(my_slot + part * EPL, EPL, w);
+            } else {
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) ss = fmaf(x[i], x[i], ss);
+                ss = sum_lanes<LPV>(ss);
+                const float n = sqrtf(ss);
+#pragma unroll
+                for (int i = 0; i < EPL; ++i)
+                    if ((signs >> i) & 1u) x[i] = -x[i];
+                fwht_local<EPL>(x);
+                fwht_lanes<EPL, LPV>(x, part);
+                // x = sqrt(d) * n * y with y = Pi k / n; compare against the
+                // boundaries scaled the same way.
+                const float u = n * sqrt_d;
+                float t[kHalf - 1];
+#pragma unroll
+                for (int j = 0; j < kHalf - 1; ++j) t[j] = pos_b[j] * u;
+                uint32_t code[EPL];
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) {
+                    const float a = fabsf(x[i]);
+                    uint32_t cnt = 0;
+#pragma unroll
+                    for (int j = 0; j < kHalf - 1; ++j) cnt += (a > t[j]) ? 1u : 0u;
+                    code[i] = x[i] > 0.f ? kHalf + cnt : kHalf - 1 - cnt;
+                }
+                uint32_t w[(EPL * KB + 31) / 32];
+                pack_codes<EPL, KB>(code, w);
+                write_u16_words(my_slot + part * (EPL * KB / 8), EPL * KB / 8, w);
+                if (part == 0)
+                    *reinterpret_cast<uint16_t*>(my_slot + S::kKeyIdxBytes) = half_bits(n);
+            }
+        }
+
+        // ---- value ---------------------------------------------------------
+        {
+            float x[EPL];
+            load_bf16<EPL>(v + vsafe * D + part * EPL, x);
+            float mn = x[0], mx = x[0];
+#pragma unroll
+            for (int i = 1; i < EPL; ++i) {
+                mn = fminf(mn, x[i]);
+                mx = fmaxf(mx, x[i]);
+            }
+            mn = min_lanes<LPV>(mn);
+            mx = max_lanes<LPV>(mx);
+            const uint16_t sb = half_bits(__fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(kTopV)));
+            const uint16_t zb = half_bits(mn);
+            const float s = half_from_bits(sb);
+            const float z = half_from_bits(zb);
+            uint32_t code[EPL];
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const float qv = __fdiv_rn(__fsub_rn(x[i], z), s);
+                const float r = fminf(fmaxf(rintf(qv), 0.f), static_cast<float>(kTopV));
+                code[i] = (s == 0.f) ? 0u : static_cast<uint32_t>(r);
+            }
+            uint32_t w[(EPL * VB + 31) / 32];
+            pack_codes<EPL, VB>(code, w);
+            write_u16_words(my_slot + S::kKeyBytes + part * (EPL * VB / 8), EPL * VB / 8, w);
+            if (part == 0) {
+                uint16_t* sz = reinterpret_cast<uint16_t*>(my_slot + S::kKeyBytes + S::kValCodeBytes);
+                sz[0] = sb;
+                sz[1] = zb;
+                if constexpr (SA > S::kBytes) my_slot[S::kBytes] = 0;
+            }
+        }
+        __syncwarp();
+
+        // ---- scatter the warp's slots ---------------------------------------
+        uint64_t dst = 0;
+        if (valid && part == 0) {
+            const int64_t t = vi / H;
+            const int h = static_cast<int>(vi - t * H);
+            const int64_t slot = slot_mapping[t];
+            if (slot >= 0) {
+                const int64_t blk = slot / c.block_size;
+                const int64_t pos = slot - blk * c.block_size;
+                if (blk < c.num_blocks)
+                    dst = reinterpret_cast<uint64_t>(c.data + blk * c.block_stride + (pos * H + h) * SA);
+                else
+                    set_flag(c.flags, kFlagSlot);
+            }
+        }
+        constexpr int kUnits = VPW * SA / 2;
+        constexpr int kPerSlot = SA / 2;
+#pragma unroll 1
+        for (int u = lane; u < (kUnits + 31) / 32 * 32; u += 32) {
+            const int vv = min(u / kPerSlot, VPW - 1);
+            const uint64_t d = __shfl_sync(kFull, dst, vv * LPV);
+            if (u < kUnits && d != 0)
+                reinterpret_cast<uint16_t*>(d)[u - vv * kPerSlot] = reinterpret_cast<const uint16_t*>(stage)[u];
+        }
+        __syncwarp();
+    }
+}
+
+template <int D, int KB, int VB>
+cudaError_t launch(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
+                   int64_t num_tokens, const int64_t* slot_mapping, int sm_count, cudaStream_t stream) {
+    constexpr int VPW = LaneSplit<D>::kVPW;
+    const int64_t vecs = num_tokens * c.num_kv_heads;
+    const int64_t warps = (vecs + VPW - 1) / VPW;
+    const int64_t want = (warps + kStoreWarps - 1) / kStoreWarps;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    store_kernel<D, KB, VB><<<grid, kStoreWarps * 32, 0, stream>>>(p, c, k, v, num_tokens, slot_mapping);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
+                          int64_t n, const int64_t* sm, int sms, cudaStream_t st) {
+    const int kb = p.kbits, vb = p.vbits;
+    if (kb == 3 && vb == 3) return launch<D, 3, 3>(p, c, k, v, n, sm, sms, st);
+    if (kb == 3 && vb == 4) return launch<D, 3, 4>(p, c, k, v, n, sm, sms, st);
+    if (kb == 4 && vb == 3) return launch<D, 4, 3>(p, c, k, v, n, sm, sms, st);
+    if (kb == 4 && vb == 4) return launch<D, 4, 4>(p, c, k, v, n, sm, sms, st);
+    if (kb == 8 && vb == 3) return launch<D, 8, 3>(p, c, k, v, n, sm, sms, st);
+    if (kb == 8 && vb == 4) return launch<D, 8, 4>(p, c, k, v, n, sm, sms, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_store(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
+                         int64_t num_tokens, const int64_t* slot_mapping, int sm_count,
+                         cudaStream_t stream) {
+    switch (p.d) {
+        case 16: return dispatch_bits<16>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
+        case 32: return dispatch_bits<32>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
+        case 64: return dispatch_bits<64>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
+        case 128: return dispatch_bits<128>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
+        case 256: return dispatch_bits<256>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace tq

@@ -284,20 +284,34 @@ def pack_bits(codes: np.ndarray, bits: int) -> np.ndarray:
     """LSB-first bitstream: code i fills bits [i*bits, (i+1)*bits) of the bytes.
 
     codes: [N, n] non-negative ints below 2**bits -> uint8 [N, ceil(n*bits/8)].
+    Eight consecutive codes fill exactly ``bits`` bytes: their integer
+    sum(code_j << (bits * j)) written little-endian.
     """
     codes = np.asarray(codes, dtype=np.int64)
     n_vec, n = codes.shape
-    shifts = np.arange(bits)
-    bitmat = ((codes[:, :, None] >> shifts[None, None, :]) & 1).astype(np.uint8)
-    bitmat = bitmat.reshape(n_vec, n * bits)
-    return np.packbits(bitmat, axis=1, bitorder="little")
+    groups = -(-n // 8)
+    padded = np.zeros((n_vec, groups * 8), dtype=np.int64)
+    padded[:, :n] = codes
+    word = np.zeros((n_vec, groups), dtype=np.int64)
+    for j in range(8):
+        word |= padded[:, j::8] << (bits * j)
+    out = np.stack([(word >> (8 * m)) & 0xFF for m in range(bits)], axis=2).astype(np.uint8)
+    return out.reshape(n_vec, groups * bits)[:, : -(-n * bits // 8)]
 
 
 def unpack_bits(data: np.ndarray, bits: int, n: int) -> np.ndarray:
     """Inverse of pack_bits: uint8 [N, nbytes] -> int64 [N, n]."""
-    bitmat = np.unpackbits(np.asarray(data, dtype=np.uint8), axis=1, bitorder="little")
-    bitmat = bitmat[:, : n * bits].reshape(-1, n, bits).astype(np.int64)
-    return (bitmat << np.arange(bits)[None, None, :]).sum(axis=2)
+    data = np.asarray(data, dtype=np.uint8)
+    n_vec = data.shape[0]
+    groups = -(-n // 8)
+    full = np.zeros((n_vec, groups * bits), dtype=np.int64)
+    full[:, : data.shape[1]] = data[:, : groups * bits]
+    full = full.reshape(n_vec, groups, bits)
+    word = np.zeros((n_vec, groups), dtype=np.int64)
+    for m in range(bits):
+        word |= full[:, :, m] << (8 * m)
+    out = np.stack([(word >> (bits * j)) & ((1 << bits) - 1) for j in range(8)], axis=2)
+    return out.reshape(n_vec, groups * 8)[:, :n]
 
 
 def f16_bytes(x: np.ndarray) -> np.ndarray:
@@ -398,9 +412,14 @@ def encode_keys_mse(k: np.ndarray, pi: np.ndarray, cb: Codebook):
     y = (k / safe[:, None]) @ pi.T
     y[n == 0] = 0.0
     b = cb.boundaries.astype(np.float64)
-    idx = np.sum(y[:, :, None] > b[None, None, :], axis=2)
-    near = np.any(np.abs(y[:, :, None] - b[None, None, :]) <= boundary_window(b, cb.sigma), axis=2)
-    return idx, n.astype(np.float16), near
+    # number of boundaries strictly below y
+    idx = np.searchsorted(b, y, side="left")
+    # the closest boundaries are the ones on either side of y
+    win = boundary_window(b, cb.sigma)
+    below = np.clip(idx - 1, 0, len(b) - 1)
+    above = np.clip(idx, 0, len(b) - 1)
+    near = (np.abs(y - b[below]) <= win[below]) | (np.abs(y - b[above]) <= win[above])
+    return idx.astype(np.int64), n.astype(np.float16), near
 
 
 def encode_values(v: np.ndarray, bits: int):
@@ -514,24 +533,26 @@ def store_kv(layer: Layer, k: np.ndarray, v: np.ndarray, slot_mapping: np.ndarra
     t_n, h_n, d = k.shape
     slots, near = encode_slots(layer, k.reshape(-1, d), v.reshape(-1, d))
     slots = slots.reshape(t_n, h_n, -1)
-    for t in range(t_n):
-        s = int(slot_mapping[t])
-        if s < 0:
-            continue
-        for h in range(h_n):
-            off = cache.slot_offset(s, h)
-            cache.data[off:off + cache.slot_bytes] = slots[t, h]
+    sm = np.asarray(slot_mapping, dtype=np.int64)
+    keep = sm >= 0
+    off = slot_offsets(cache, sm[keep])
+    cache.data[off[..., None] + np.arange(cache.slot_bytes)] = slots[keep]
     return near.reshape(t_n, h_n, d)
+
+
+def slot_offsets(cache: PagedCache, slots: np.ndarray) -> np.ndarray:
+    """Byte offsets [T, H] of every KV head's slot for the given slot ids."""
+    blk, pos = np.divmod(np.asarray(slots, dtype=np.int64), cache.block_size)
+    heads = np.arange(cache.num_kv_heads)
+    return (blk * cache.block_stride)[:, None] + (pos[:, None] * cache.num_kv_heads + heads[None, :]) * cache.slot_bytes
 
 
 def read_slots(cache: PagedCache, block_table_row: np.ndarray, seq_len: int, head: int) -> np.ndarray:
     """Bytes of one KV head's slots for positions 0..seq_len-1 of a sequence."""
-    out = np.empty((seq_len, cache.slot_bytes), dtype=np.uint8)
-    for j in range(seq_len):
-        blk = int(block_table_row[j // cache.block_size])
-        off = blk * cache.block_stride + ((j % cache.block_size) * cache.num_kv_heads + head) * cache.slot_bytes
-        out[j] = cache.data[off:off + cache.slot_bytes]
-    return out
+    pos = np.arange(seq_len)
+    slots = np.asarray(block_table_row, dtype=np.int64)[pos // cache.block_size] * cache.block_size + pos % cache.block_size
+    off = slot_offsets(cache, slots)[:, head]
+    return cache.data[off[:, None] + np.arange(cache.slot_bytes)]
 
 
 # ---------------------------------------------------------------------------

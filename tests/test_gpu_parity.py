@@ -1,0 +1,202 @@
+"""CUDA path against the CPU oracle on the same seeded inputs.
+
+Store: packed bytes bit-exact (values, FP8 keys), key indices bit-exact
+outside the near-boundary window, vec_norm bit-exact outside the fp16
+midpoint window.  Decode: per output row max |o - r| <= 2e-3 max |r|,
+where the GPU decodes the oracle's own cache bytes (small cases) or its own
+cache (full sizes, sampled rows).  Dequant: values bit-exact in bf16, keys
+within one bf16 ulp.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kv_cache_quantization_store_gb300 as tq
+import oracle as O
+from kv_cache_quantization_store_gb300 import workloads as W
+from tq_gpu_util import (assert_rows_close, bf16, compare_slots, gpu_cache_for, gpu_decode, gpu_store, host_cfg,
+                         oracle_cache, oracle_layer, slot_bytes, upload_cache)
+
+pytestmark = pytest.mark.gpu
+
+
+def small_cases():
+    return [
+        W.named("c0"),
+        W.small("c1", [1, 15, 16, 17, 250, 700]),
+        W.small("c2", [33, 513, 2]),
+        W.small("c3", [1000, 77]),
+        W.small("c4", [600, 31], layers=(2,)),
+        W.custom(16, 3, 3, False, 2, 2, 16, [40, 3], 2001),
+        W.custom(32, 4, 3, True, 1, 8, 32, [100], 2002),
+        W.custom(64, 4, 3, True, 4, 20, 16, [65, 130, 5], 2003),
+        W.custom(128, 8, 3, False, 3, 6, 16, [90, 47], 2004, kv_mode="lognormal"),
+        W.custom(256, 8, 4, False, 2, 16, 48, [200], 2005),
+        W.custom(256, 3, 3, True, 1, 1, 16, [77], 2006, kv_mode="outliers"),
+        W.custom(128, 4, 4, False, 8, 64, 64, [300, 129], 2007),
+    ]
+
+
+CASES = small_cases()
+IDS = [f"{w.name}-{'x'.join(map(str, w.seq_lens))}" for w in CASES]
+
+
+@pytest.mark.parametrize("wl", CASES, ids=IDS)
+def test_store_parity(cuda_device, wl):
+    layer_idx = wl.layers[-1]
+    k, v = wl.kv()
+    cfg, cache = gpu_store(wl, layer_idx, cuda_device, k, v)
+    layer = oracle_layer(wl, layer_idx)
+    ocache, near = oracle_cache(wl, layer, k, v)
+    assert cache.error_flags() == 0
+    flat = cache.data.cpu().numpy()
+    sm = wl.slot_mapping()
+    got = slot_bytes(flat, wl, cfg.slot_size_aligned, sm).reshape(-1, cfg.slot_size_aligned)
+    want = slot_bytes(ocache.data, wl, cfg.slot_size_aligned, sm).reshape(-1, cfg.slot_size_aligned)
+    stats = compare_slots(layer, got, want, near.reshape(-1, wl.head_dim), k.reshape(-1, wl.head_dim))
+    assert stats["index_exempt"] <= max(2, got.shape[0] * wl.head_dim // 100000)
+    # bytes outside written slots stay zero
+    written = np.zeros(flat.shape, dtype=bool)
+    idx = slot_bytes(np.arange(flat.size), wl, cfg.slot_size_aligned, sm)
+    written[idx.ravel()] = True
+    assert not flat[~written].any()
+
+
+@pytest.mark.parametrize("wl", CASES, ids=IDS)
+def test_decode_parity(cuda_device, wl):
+    layer_idx = wl.layers[-1]
+    k, v = wl.kv()
+    layer = oracle_layer(wl, layer_idx)
+    ocache, _ = oracle_cache(wl, layer, k, v)
+    cfg = host_cfg(wl)
+    cache = upload_cache(ocache, cfg, layer_idx, cuda_device)
+    q = wl.q()
+    table = wl.layout()[0]
+    want = O.decode_attention(layer, q, ocache, table, wl.seq_lens)
+    for splits in (0, 1, 3):
+        got = gpu_decode(wl, cfg, cache, q, cuda_device, num_splits=splits)
+        assert_rows_close(got, want)
+    assert cache.error_flags() == 0
+
+
+@pytest.mark.parametrize("wl", CASES[:6], ids=IDS[:6])
+def test_decode_split_invariance(cuda_device, wl):
+    k, v = wl.kv()
+    cfg, cache = gpu_store(wl, 0, cuda_device, k, v)
+    q = wl.q()
+    ref = gpu_decode(wl, cfg, cache, q, cuda_device, num_splits=1)
+    max_chunks = math.ceil(int(wl.seq_lens.max()) / 16)
+    for splits in sorted({2, 7, max_chunks, 0}):
+        got = gpu_decode(wl, cfg, cache, q, cuda_device, num_splits=splits)
+        assert_rows_close(got, ref, rtol=2e-5)
+
+
+@pytest.mark.parametrize("wl", CASES, ids=IDS)
+def test_dequant_parity(cuda_device, wl):
+    layer_idx = wl.layers[-1]
+    k, v = wl.kv()
+    layer = oracle_layer(wl, layer_idx)
+    ocache, _ = oracle_cache(wl, layer, k, v)
+    cfg = host_cfg(wl)
+    cache = upload_cache(ocache, cfg, layer_idx, cuda_device)
+    table = wl.layout()[0]
+    cu = wl.cu_seqlens()
+    rows = int(cu[-1])
+    k_out = torch.full((rows, wl.num_kv_heads, wl.head_dim), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+    v_out = torch.full_like(k_out, float("nan"))
+    tq.tq_dequant(cfg, cache, torch.from_numpy(table).to(cuda_device), torch.from_numpy(cu).to(cuda_device),
+                  int(wl.seq_lens.max()), k_out, v_out)
+    torch.cuda.synchronize()
+    kw, vw = O.dequant_cache(layer, ocache, table, cu)
+    kg = k_out.float().cpu().numpy()
+    vg = v_out.float().cpu().numpy()
+    np.testing.assert_array_equal(vg, vw)
+    tol = np.abs(kw) * 2.0 ** -7 + 1e-6 * np.abs(kw).max(axis=-1, keepdims=True)
+    assert np.all(np.abs(kg - kw) <= tol)
+
+
+def test_fp8_keys_exhaustive_bf16(cuda_device):
+    """All finite bf16 bit patterns as FP8 keys (d=128, 512 vectors)."""
+    pat = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        x = (pat << 16).view(np.float32)
+    x = np.where(np.isfinite(x) | np.isinf(x), x, 0).astype(np.float32)
+    wl = W.custom(128, 8, 4, False, 1, 1, 16, [512], 2100)
+    k = x.reshape(512, 1, 128)
+    _, v = wl.kv()
+    cfg, cache = gpu_store(wl, 0, cuda_device, k, v)
+    got = slot_bytes(cache.data.cpu().numpy(), wl, cfg.slot_size_aligned, wl.slot_mapping()).reshape(512, -1)
+    want = O.e4m3_encode(k.reshape(-1)).reshape(512, 128)
+    np.testing.assert_array_equal(got[:, :128], want)
+
+
+def test_negative_and_out_of_range_slots(cuda_device):
+    wl = W.custom(64, 3, 4, False, 2, 4, 16, [64], 2200)
+    k, v = wl.kv()
+    sm = wl.slot_mapping().copy()
+    sm[5] = -1
+    sm[9] = 10 ** 9  # beyond the cache: skipped and flagged
+    cfg, cache = gpu_store(wl, 0, cuda_device, k, v, slots=sm)
+    assert cache.error_flags() & tq.TQ_FLAG_SLOT_OUT_OF_RANGE
+    layer = oracle_layer(wl, 0)
+    keep = np.ones(64, dtype=bool)
+    keep[[5, 9]] = False
+    ocache = O.new_cache(layer.cfg, wl.layout()[1], wl.block_size, wl.num_kv_heads)
+    near = O.store_kv(layer, k, v, np.where(keep, sm, -1), ocache)
+    flat = cache.data.cpu().numpy()
+    orig = wl.slot_mapping()
+    assert not slot_bytes(flat, wl, cfg.slot_size_aligned, orig[~keep]).any()
+    got = slot_bytes(flat, wl, cfg.slot_size_aligned, orig[keep]).reshape(-1, cfg.slot_size_aligned)
+    want = slot_bytes(ocache.data, wl, cfg.slot_size_aligned, orig[keep]).reshape(-1, cfg.slot_size_aligned)
+    compare_slots(layer, got, want, near[keep].reshape(-1, 64), k[keep].reshape(-1, 64))
+
+
+def test_decode_flags_bad_block_and_length(cuda_device):
+    wl = W.custom(64, 3, 4, False, 1, 2, 16, [48, 20], 2300)
+    k, v = wl.kv()
+    cfg, cache = gpu_store(wl, 0, cuda_device, k, v)
+    table = wl.layout()[0].copy()
+    table[0, 1] = 10 ** 6
+    out = gpu_decode(wl, cfg, cache, wl.q(), cuda_device, table=table)
+    assert np.all(np.isfinite(out))
+    assert cache.error_flags() & tq.TQ_FLAG_BLOCK_OUT_OF_RANGE
+    cache.flags.zero_()
+    out = gpu_decode(wl, cfg, cache, wl.q(), cuda_device, seq_lens=[48, 20], max_seq_len=32)
+    assert np.all(np.isfinite(out))
+    assert cache.error_flags() & tq.TQ_FLAG_SEQ_TOO_LONG
+
+
+def test_padded_block_stride(cuda_device):
+    """The lcm page geometry read the other way: 16-token blocks padded to
+    the 536576-byte unified page (4bit_nc, d=256, 4 KV heads)."""
+    base = W.named("c4")
+    cfg = host_cfg(base)
+    page, _ = tq.tq_hybrid_page(cfg, 4, 2)
+    wl = W.custom(256, 4, 4, True, 4, 16, 16, [70, 33], 2400, block_stride=page)
+    k, v = wl.kv()
+    cfg, cache = gpu_store(wl, 1, cuda_device, k, v)
+    layer = oracle_layer(wl, 1)
+    ocache, near = oracle_cache(wl, layer, k, v)
+    flat = cache.data.cpu().numpy()
+    sm = wl.slot_mapping()
+    got = slot_bytes(flat, wl, cfg.slot_size_aligned, sm).reshape(-1, cfg.slot_size_aligned)
+    want = slot_bytes(ocache.data, wl, cfg.slot_size_aligned, sm).reshape(-1, cfg.slot_size_aligned)
+    compare_slots(layer, got, want, near.reshape(-1, 256), k.reshape(-1, 256))
+    q = wl.q()
+    want_out = O.decode_attention(layer, q, ocache, wl.layout()[0], wl.seq_lens)
+    dev = upload_cache(ocache, cfg, 1, cuda_device)
+    assert_rows_close(gpu_decode(wl, cfg, dev, q, cuda_device), want_out)
+
+
+def test_empty_inputs(cuda_device):
+    wl = W.custom(64, 3, 4, False, 1, 2, 16, [16], 2500)
+    cfg = host_cfg(wl)
+    cache = gpu_cache_for(wl, cfg, 0, cuda_device)
+    empty = torch.empty((0, 1, 64), dtype=torch.bfloat16, device=cuda_device)
+    tq.tq_store_kv(cfg, empty, empty, torch.empty(0, dtype=torch.int64, device=cuda_device), cache)
+    torch.cuda.synchronize()
+    assert not cache.data.any()
+    out = gpu_decode(wl, cfg, cache, wl.q(), cuda_device, seq_lens=[0])
+    assert np.all(out == 0)
