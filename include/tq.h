@@ -241,6 +241,37 @@ TQ_API tq_status tq_dequant(const tq_config* cfg, const tq_cache* cache, const i
 TQ_API tq_status tq_hybrid_page(const tq_config* cfg, int32_t num_kv_heads, int32_t skip_dtype_bytes,
                                 int64_t* page_bytes_out, int32_t* tokens_per_page_out);
 
+/*
+ * tq_decode_attention_noalloc -- the same decode as tq_decode_attention, for
+ * callers that cannot allocate device memory for its workspace.  The pages
+ * have no counterpart: they do not discuss how decode scratch is allocated.
+ *
+ * Who needs it: a serving engine that gave nearly all free device memory to
+ * its KV-cache pool at start-up (a later cudaMalloc fails); a plugin inside a
+ * host application that owns every device allocation; real-time code that
+ * cannot accept the device-wide synchronisation of cudaMalloc / cudaFree.
+ *
+ * Instead of a caller workspace it uses a fixed scratch array of
+ * TQ_NOALLOC_SCRATCH_BYTES in the library's static device memory, which every
+ * GPU that loads the library holds until the process exits.  It allocates
+ * nothing and calls no cudaMalloc or cudaFree.
+ *   - Arguments, layouts and results are those of tq_decode_attention.
+ *   - A decode whose workspace (tq_decode_workspace_size) exceeds the limit is
+ *     rejected with TQ_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents: calls that overlap on the GPU (other streams, other host
+ *     threads) race and give wrong results.  Serialise them.
+ */
+#define TQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+TQ_API tq_status tq_decode_attention_noalloc(const tq_config* cfg, const void* q_dev, int32_t num_seqs,
+                                             int32_t num_q_heads, const tq_cache* cache,
+                                             const int32_t* block_table_dev, int32_t max_blocks_per_seq,
+                                             const int32_t* seq_lens_dev, int32_t max_seq_len, float sm_scale,
+                                             int32_t num_splits, float* out_dev, void* stream);
+
 /* Static text naming a status. */
 TQ_API const char* tq_status_str(tq_status status);
 

@@ -19,13 +19,15 @@ import torch
 __all__ = [
     "TQError", "TqConfig", "TqCache", "PagedCache", "lib", "library_path",
     "tq_config_init", "tq_config_from_preset", "tq_layer_signs", "tq_store_kv",
-    "tq_decode_workspace_size", "tq_decode_attention", "tq_dequant", "tq_status_str",
+    "tq_decode_workspace_size", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_dequant",
+    "tq_status_str", "TQ_NOALLOC_SCRATCH_BYTES",
     "new_paged_cache", "tq_hybrid_page", "PRESETS",
 ]
 
 PRESETS = ("turboquant_k8v4", "turboquant_4bit_nc", "turboquant_k3v4_nc", "turboquant_3bit_nc")
 
 TQ_OK = 0
+TQ_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # include/tq.h
 TQ_FLAG_SLOT_OUT_OF_RANGE = 1
 TQ_FLAG_BLOCK_OUT_OF_RANGE = 2
 TQ_FLAG_SEQ_TOO_LONG = 4
@@ -103,6 +105,11 @@ _SIGNATURES = {
     "tq_dequant": (ctypes.c_int, [ctypes.POINTER(TqConfig), ctypes.POINTER(TqCache), ctypes.c_void_p,
                                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "tq_decode_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(TqConfig), ctypes.c_void_p, ctypes.c_int32,
+                                                   ctypes.c_int32, ctypes.POINTER(TqCache), ctypes.c_void_p,
+                                                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+                                                   ctypes.c_float, ctypes.c_int32, ctypes.c_void_p,
+                                                   ctypes.c_void_p]),
     "tq_hybrid_page": (ctypes.c_int, [ctypes.POINTER(TqConfig), ctypes.c_int32, ctypes.c_int32,
                                       ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
@@ -261,6 +268,25 @@ def tq_decode_attention(cfg: TqConfig, q: torch.Tensor, cache: PagedCache, block
         _dev(seq_lens, torch.int32, "seq_lens"), int(max_seq_len), float(sm_scale), int(num_splits),
         _dev(out, torch.float32, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
         _stream(stream)))
+
+
+def tq_decode_attention_noalloc(cfg: TqConfig, q: torch.Tensor, cache: PagedCache, block_table: torch.Tensor,
+                                seq_lens: torch.Tensor, max_seq_len: int, out: torch.Tensor, sm_scale: float = 0.0,
+                                num_splits: int = 0, stream=None):
+    """tq_decode_attention without a workspace argument, for callers that
+    cannot allocate device memory: it runs on the library's fixed static
+    scratch (see tq_decode_attention_noalloc in include/tq.h for the size
+    limit and why overlapping calls race)."""
+    if q.dim() != 3 or q.shape[2] != cfg.head_dim or out.shape != q.shape:
+        raise ValueError("q and out must be [num_seqs, num_q_heads, head_dim]")
+    if block_table.dim() != 2 or block_table.shape[0] != q.shape[0] or seq_lens.shape != (q.shape[0],):
+        raise ValueError("block_table must be [S, max_blocks] and seq_lens [S]")
+    desc = cache.descriptor()
+    _check(lib().tq_decode_attention_noalloc(
+        ctypes.byref(cfg), _dev(q, torch.bfloat16, "q"), q.shape[0], q.shape[1], ctypes.byref(desc),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _dev(seq_lens, torch.int32, "seq_lens"), int(max_seq_len), float(sm_scale), int(num_splits),
+        _dev(out, torch.float32, "out"), _stream(stream)))
 
 
 def tq_dequant(cfg: TqConfig, cache: PagedCache, block_table: torch.Tensor, cu_seqlens: torch.Tensor,

@@ -165,6 +165,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 }  // namespace
 
+void tq::set_last_error(const char* msg) { std::snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 extern "C" {
 
 const char* tq_status_str(tq_status s) {

@@ -64,6 +64,9 @@ cudaError_t launch_dequant(const LayerParams& p, const CacheGeom& c, const int32
                            int max_blocks_per_seq, const int32_t* cu_seqlens, int num_seqs,
                            int max_seq_len, uint16_t* k_out, uint16_t* v_out, cudaStream_t stream);
 
+// Records the text tq_last_error() returns on this host thread.
+void set_last_error(const char* msg);
+
 // Supported compile-time shapes.
 inline bool supported_head_dim(int d) {
     return d == 16 || d == 32 || d == 64 || d == 128 || d == 256;
