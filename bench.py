@@ -51,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="c4", help="c1 | c2 | c3 | c4 (c4 is the reported configuration)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--layers", type=int, default=None, help="use only the first N layers (profiling)")
+    ap.add_argument("--seqs", type=int, default=None, help="decode only the first N sequences (profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
@@ -224,7 +226,7 @@ def run_ours(args):
     if rank == 0:
         tq_build.build()
     barrier()
-    wl = W.named(args.workload)
+    wl = shrink(W.named(args.workload), args)
     cfg = tq.tq_config_init(wl.head_dim, wl.key_bits, wl.value_bits, wl.norm_correction, wl.seed)
     slot_al = cfg.slot_size_aligned
     table_np, nblk = wl.layout()
@@ -347,6 +349,21 @@ def run_ours(args):
         result["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def shrink(wl, args):
+    """A reduced copy of the workload for profiling runs (fewer layers and
+    decode sequences); the full configuration is the default."""
+    if args.layers:
+        wl.layers = tuple(wl.layers[: args.layers])
+    if args.seqs:
+        wl.seq_lens = wl.seq_lens[: args.seqs]
+        if wl.store_tokens:
+            wl.store_tokens = min(wl.store_tokens, int(wl.seq_lens.sum()))
+        wl.description += f" [reduced: {len(wl.layers)} layer(s), {args.seqs} sequences]"
+    elif args.layers:
+        wl.description += f" [reduced: {len(wl.layers)} layer(s)]"
+    return wl
 
 
 def run_e2e(args, tq, wl, cfg, caches, k_new, v_new, slots_new, q, table, lens, max_len, ws, outs, stream,

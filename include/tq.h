@@ -190,8 +190,9 @@ TQ_API size_t tq_decode_workspace_size(const tq_config* cfg, int32_t num_seqs, i
  * the FP8 key, and v_hat = scale * code + zero.  Keys are never expanded: the
  * query is rotated once (Pi q) and scored against centroids.  The history is
  * cut into num_splits ranges (0 = chosen from the SM count) whose partial
- * softmax states are merged by log-sum-exp; the result does not depend on the
- * split count beyond fp32 rounding.
+ * softmax states are merged by log-sum-exp; the result depends on the split
+ * count only through rounding (the tensor-core path rounds the softmax
+ * weights to fp16 relative to each split's running maximum).
  *   q_dev: bf16 [num_seqs, num_q_heads, head_dim]; num_q_heads % num_kv_heads == 0
  *   block_table_dev: int32 [num_seqs, max_blocks_per_seq]
  *   seq_lens_dev: int32 [num_seqs]; each <= max_seq_len; 0 gives a zero row

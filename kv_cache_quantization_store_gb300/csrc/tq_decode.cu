@@ -340,9 +340,7 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const DecodeArgs& a
     decode_kernel<D, KB, VB><<<grid, kThreads, lay.total, stream>>>(p, c, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 cgrid(static_cast<unsigned>(a.num_q_heads), static_cast<unsigned>(num_seqs));
-    combine_kernel<<<cgrid, D < 128 ? 128 : D, 0, stream>>>(a.partials, out, a.num_q_heads, D, a.num_splits);
-    return cudaGetLastError();
+    return launch_combine(a.partials, out, num_seqs, a.num_q_heads, D, a.num_splits, stream);
 }
 
 template <int D>
@@ -359,6 +357,13 @@ cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const Decode
 }
 
 }  // namespace
+
+cudaError_t launch_combine(const float* partials, float* out, int num_seqs, int num_q_heads, int d,
+                           int num_splits, cudaStream_t stream) {
+    dim3 cgrid(static_cast<unsigned>(num_q_heads), static_cast<unsigned>(num_seqs));
+    combine_kernel<<<cgrid, d < 128 ? 128 : d, 0, stream>>>(partials, out, num_q_heads, d, num_splits);
+    return cudaGetLastError();
+}
 
 DecodePlan plan_decode(const LayerParams& p, int num_seqs, int num_q_heads, int num_kv_heads, int max_seq_len,
                        int num_splits_req, int sm_count) {
@@ -388,6 +393,9 @@ cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16
                           int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
                           const int32_t* seq_lens, int max_seq_len, float sm_scale, const DecodePlan& plan,
                           float* out, void* workspace, cudaStream_t stream) {
+    if (decode_mma_supported(p, c.num_kv_heads, num_q_heads))
+        return launch_decode_mma(p, c, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq, seq_lens,
+                                 max_seq_len, sm_scale, plan, out, workspace, stream);
     DecodeArgs a{};
     a.q = q;
     a.block_table = block_table;

@@ -60,6 +60,16 @@ cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16
                           const int32_t* seq_lens, int max_seq_len, float sm_scale,
                           const DecodePlan& plan, float* out, void* workspace, cudaStream_t stream);
 
+// Tensor-core decode (tq_decode_mma.cu): H in {1,2,4,8}, G <= 8, d in {64,128,256}.
+bool decode_mma_supported(const LayerParams& p, int num_kv_heads, int num_q_heads);
+cudaError_t launch_decode_mma(const LayerParams& p, const CacheGeom& c, const uint16_t* q, int num_seqs,
+                              int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                              const int32_t* seq_lens, int max_seq_len, float sm_scale, const DecodePlan& plan,
+                              float* out, void* workspace, cudaStream_t stream);
+// Log-sum-exp merge of split partials [S, Hq, splits, d + 2] into out [S, Hq, d].
+cudaError_t launch_combine(const float* partials, float* out, int num_seqs, int num_q_heads, int d,
+                           int num_splits, cudaStream_t stream);
+
 cudaError_t launch_dequant(const LayerParams& p, const CacheGeom& c, const int32_t* block_table,
                            int max_blocks_per_seq, const int32_t* cu_seqlens, int num_seqs,
                            int max_seq_len, uint16_t* k_out, uint16_t* v_out, cudaStream_t stream);
