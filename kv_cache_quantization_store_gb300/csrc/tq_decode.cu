@@ -365,17 +365,53 @@ cudaError_t launch_combine(const float* partials, float* out, int num_seqs, int 
     return cudaGetLastError();
 }
 
+// Resident CTAs per SM of the CUDA-core decode for these shapes.
+int v1_ctas_per_sm(const LayerParams& p, int num_kv_heads, int num_q_heads) {
+    int ctas = 0;
+    auto query = [&](auto kern) {
+        const SmemLayout lay(num_q_heads, p.d, num_kv_heads, p.slot_al);
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) != cudaSuccess) return;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, kern, kThreads, lay.total) != cudaSuccess) ctas = 0;
+    };
+    // every instantiation of a head size has the same shared memory and near the same registers
+    switch (p.d) {
+        case 16: query(decode_kernel<16, 4, 4>); break;
+        case 32: query(decode_kernel<32, 4, 4>); break;
+        case 64: query(decode_kernel<64, 4, 4>); break;
+        case 128: query(decode_kernel<128, 4, 4>); break;
+        case 256: query(decode_kernel<256, 4, 4>); break;
+        default: break;
+    }
+    return ctas;
+}
+
 DecodePlan plan_decode(const LayerParams& p, int num_seqs, int num_q_heads, int num_kv_heads, int max_seq_len,
                        int num_splits_req, int sm_count) {
-    (void)num_kv_heads;
     DecodePlan plan{};
     const int max_chunks = (max_seq_len + kTokPerChunk - 1) / kTokPerChunk;
-    int splits;
+    int splits = 1;
     if (num_splits_req > 0) {
         splits = num_splits_req;
-    } else {
-        const int target = 2 * (sm_count > 0 ? sm_count : 1);
-        splits = num_seqs > 0 ? (target + num_seqs - 1) / num_seqs : 1;
+    } else if (num_seqs > 0 && max_chunks > 0) {
+        // Pick the split count that finishes soonest: CTAs run in waves of
+        // sm_count * (resident CTAs per SM); each CTA costs its chunks plus a
+        // fixed prologue (tables, query rotation) worth about kPrologue chunks.
+        constexpr int kPrologue = 4;
+        int per_sm = decode_mma_supported(p, num_kv_heads, num_q_heads)
+                         ? decode_mma_ctas_per_sm(p, num_kv_heads, num_q_heads)
+                         : v1_ctas_per_sm(p, num_kv_heads, num_q_heads);
+        if (per_sm < 1) per_sm = 1;
+        const long long capacity = static_cast<long long>(sm_count > 0 ? sm_count : 1) * per_sm;
+        long long best_cost = -1;
+        const int limit = max_chunks < 512 ? max_chunks : 512;
+        for (int cand = 1; cand <= limit; ++cand) {
+            const long long waves = (static_cast<long long>(num_seqs) * cand + capacity - 1) / capacity;
+            const long long cost = waves * (kPrologue + (max_chunks + cand - 1) / cand);
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                splits = cand;
+            }
+        }
     }
     if (splits > max_chunks) splits = max_chunks;
     if (splits < 1) splits = 1;

@@ -1,0 +1,754 @@
+// Fused decode attention on the packed cache with tensor-core QK and P.V
+// (mma.sync m16n8k16, f16 operands, f32 accumulation).  Kernel template;
+// tq_decode_mma_d{64,128,256}.cu instantiate it per head size.
+//
+// [ART] hnwysp.cn TurboQuant article, "Direction 1": rotate the query once
+// (q' = Pi q) and score it against the compressed keys; run an online
+// softmax block by block; never materialise fp16 K or V.  [TQC]
+// TurboQuantConfig docstring, norm_correction: divide each score by the
+// norm of its centroid vector.
+//
+// Work decomposition.  A CTA owns one sequence's split (a range of 16-token
+// chunks) and has WPH warps per KV head (H heads, compile-time).  Each chunk
+// -- 16 consecutive tokens of every head, contiguous and 16-byte aligned in a
+// paged block -- is staged into shared memory with 16-byte cp.async copies
+// through an NS-deep ring whose stage slots and per-thread offsets are
+// compile-time constants.  The WPH warps of a head split its dims: each
+// computes a partial QK over its share, the partials are added through
+// shared memory, and each computes P.V for its share of the output.
+//
+//   QK   S[16 tok x 8 q] = Khat[16 x d] * Q'^T[d x 8]
+//        Thread (r = lane/4, c = lane%4) feeds key dims of tokens r and
+//        r+8; each A register is one pair of consecutive dims, looked up
+//        from a per-lane-replicated pair table in shared memory (3-bit: 64
+//        entries of {half2 c, float c0^2+c1^2}; 4-bit: 256 entries of half2
+//        c), or converted from two FP8 bytes.  Q' is permuted to the same dim
+//        order and split into fp16 hi + lo parts (two MMAs), and the table
+//        holds the centroids times a scale chosen so that their fp16 rounding
+//        error is small; together they keep the scores near fp32 accuracy.
+//   norm 3-bit: the table's squared sums; 4-bit: Khat*Khat (HMUL2) against a
+//        ones column, one extra MMA per k-step.
+//   softmax  per query column, lazily rescaled (only when the running max
+//        grows by more than 2^8).
+//   PV   O^T[d x 8 q] += V^T[d x 16 tok] * P'[16 tok x 8 q], P' = p * scale_t.
+//        Thread r feeds value dims of tokens 2c, 2c+1, 2c+8, 2c+9 as fp16
+//        1 + code / 2^VB (bit placement, no conversion); an extra M-tile
+//        whose row 0 is all ones accumulates sum P', which removes the +1
+//        exactly and re-centres the codes on the middle of their range.  P
+//        moves into the B layout with movmatrix.  The zero points enter as
+//        sum p * (zero_t + centre * scale_t) in fp32.
+//
+// Each warp writes its dims of a partial (m, l, o) per query head; the
+// combine kernel merges the splits by log-sum-exp.  Every call writes every
+// partial it reads, so the workspace needs no clearing between calls.
+#pragma once
+
+#include <cmath>
+#include <type_traits>
+
+#include "tq_device.cuh"
+
+namespace tq {
+namespace mma {
+
+constexpr int kTok = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct Args {
+    const uint16_t* q;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    float* partials;
+    int num_q_heads;
+    int max_blocks;
+    int max_seq_len;
+    int chunks_per_split;
+    int num_splits;
+    float qscale;     // sm_scale * log2(e)
+    float lut_scale;  // table value = centroid * lut_scale (= gamma * sqrt(d))
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Two fp32 values -> f16x2 (lo = first element, hi = second).
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ void group_barrier(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Shared-memory loads through generic pointers into the dynamic shared array.
+__device__ __forceinline__ uint32_t ld32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint16_t ld16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
+
+// NW consecutive little-endian words starting at any byte address of shared
+// memory (reads one aligned word past the range; the ring carries padding).
+template <int NW>
+__device__ __forceinline__ void ld_words(const uint8_t* p, uint32_t (&w)[NW]) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint8_t* base = p - (a & 3u);
+    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
+    uint32_t raw[NW + 1];
+#pragma unroll
+    for (int i = 0; i <= NW; ++i) raw[i] = ld32(base + 4 * i);
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
+}
+
+// Value codes of local dim n for two tokens as f16x2: 1 + code / 2^VB,
+// tokens a in the low half and b in the high half.
+template <int VB, int NW>
+__device__ __forceinline__ uint32_t value_pair(const uint32_t (&wa)[NW], const uint32_t (&wb)[NW], int n) {
+    constexpr int kPlace = 10 - VB;  // code lands in mantissa bits [kPlace, 10)
+    constexpr uint32_t kMask = ((1u << VB) - 1u) << kPlace;
+    const int bit = n * VB;
+    int b0;  // first byte of a 16-bit window that holds the field
+    if ((bit % 16) + VB <= 16) b0 = 2 * (bit / 16);
+    else b0 = bit / 8;
+    uint32_t win;
+    if (b0 % 4 <= 2) {
+        const int o = b0 % 4;
+        const uint32_t sel = o | ((o + 1) << 4) | ((o + 4) << 8) | ((o + 5) << 12);
+        win = prmt(wa[b0 / 4], wb[b0 / 4], sel);
+    } else {
+        const uint32_t fa = __funnelshift_r(wa[b0 / 4], wa[b0 / 4 + 1], 24);
+        const uint32_t fb = __funnelshift_r(wb[b0 / 4], wb[b0 / 4 + 1], 24);
+        win = prmt(fa, fb, 0x5410);
+    }
+    const int pos = bit - 8 * b0;  // field position inside each 16-bit half
+    const int sh = kPlace - pos;
+    const uint32_t x = sh >= 0 ? (win << sh) : (win >> (-sh));
+    return (x & (kMask | (kMask << 16))) | 0x3C003C00u;
+}
+
+// Compile-time geometry of one kernel instantiation.  Shared memory:
+// [pair table][score exchange][16 zero bytes][stage ring][Q' fragments].
+template <int D, int KB, int VB, int H, int WPH, int NS>
+struct Geo {
+    using S = Slot<D, KB, VB>;
+    static constexpr int SA = S::kAligned;
+    static constexpr int ROW = H * SA;        // one token, all heads
+    static constexpr int CHUNK = kTok * ROW;  // one stage
+    static constexpr int STAGE = (CHUNK + 15) & ~15;
+    static constexpr int NWARPS = H * WPH;
+    static constexpr int NT = 32 * NWARPS;
+    static constexpr int KSTEPS = D / 16 / WPH;  // k-steps of one warp
+    static constexpr int MTILES = D / 16 / WPH;  // M-tiles of one warp
+    static constexpr int KBYTES = (D / 4) * KB / 8;  // key code bytes of one thread, one token
+    static constexpr int KBYTES_W = KBYTES / WPH;    // ... of which one warp reads
+    static constexpr int KWORDS = (KBYTES_W + 3) / 4;
+    static constexpr int VBITS_W = (D / 8 / WPH) * VB;  // value code bits of one thread, token and warp
+    static constexpr int VWORDS = (VBITS_W + 31) / 32;
+    static constexpr int LUT_ENTRY = KB == 3 ? 8 : 4;
+    static constexpr int LUT_ENTRIES = KB == 3 ? 64 : (KB == 4 ? 256 : 0);
+    static constexpr int LUT_BYTES = LUT_ENTRIES * 32 * LUT_ENTRY;
+    static constexpr int XCH_W = WPH > 1 ? 32 * 8 * 4 : 0;
+    static constexpr int X_OFF = LUT_BYTES;
+    static constexpr int ZERO_OFF = X_OFF + NWARPS * XCH_W;
+    static constexpr int RING_OFF = ZERO_OFF + 16;
+    static constexpr int RING = NS * STAGE + 16;
+    // Q' fragments follow the ring: per warp, k-step and query row r < G,
+    // 4 lanes x {hi0, hi1, lo0, lo1}, i.e. G * d * 4 bytes per KV head.
+    __host__ __device__ static int q_off(int hq) {
+        const int qrot = hq * D * 4;  // the ring also holds the fp32 query rotation
+        return RING_OFF + (RING > qrot ? RING : qrot);
+    }
+    __host__ __device__ static int smem_bytes(int hq) { return q_off(hq) + hq * D * 4; }
+};
+
+template <int D, int KB, int VB, bool NC, int H, int WPH, int NS, int MINB>
+__global__ void __launch_bounds__(32 * H * WPH, MINB)
+decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
+    using G = Geo<D, KB, VB, H, WPH, NS>;
+    using S = typename G::S;
+    static_assert(((D / 4 / WPH) * KB) % 8 == 0 && ((D / 8 / WPH) * VB) % 8 == 0,
+                  "a warp's share of the codes must start on a byte");
+    constexpr int SA = G::SA;
+    constexpr int ROW = G::ROW;
+    constexpr int NT = G::NT;
+    constexpr float kValW = static_cast<float>(1 << VB);  // 1 / weight of a code in the fp16 operand
+    constexpr float kCentre = 0.5f * static_cast<float>((1 << VB) - 1);
+    extern __shared__ __align__(16) uint8_t smem[];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int r = lane >> 2;
+    const int cc = lane & 3;
+    const int Hq = a.num_q_heads;
+    const int Gq = Hq / H;
+    const int h = warp / WPH;     // KV head of this warp
+    const int part = warp % WPH;  // its share of the head's dims
+    const int split = blockIdx.x;
+    const int s = blockIdx.y;
+    uint8_t* const ring = smem + G::RING_OFF;
+    const uint32_t ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+
+    // ---- sequence range ------------------------------------------------------
+    int L = a.seq_lens[s];
+    const int cap = min(a.max_seq_len, a.max_blocks * c.block_size);
+    if (L > cap || L < 0) {
+        if (threadIdx.x == 0 && split == 0) set_flag(c.flags, kFlagSeq);
+        L = L < 0 ? 0 : cap;
+    }
+    const int n_chunks = (L + kTok - 1) / kTok;
+    const int c0 = split * a.chunks_per_split;
+    const int c1 = min(c0 + a.chunks_per_split, n_chunks);
+
+    // ---- pair lookup table: centroids * lut_scale as fp16, one copy per lane ----
+    const float ls = a.lut_scale;
+    if constexpr (KB == 3) {
+        // 64 entries x 32 lanes x 8 bytes; one 16-byte store writes two lanes' copies
+        for (int i = threadIdx.x; i < 64 * 16; i += NT) {
+            const int e = i >> 4;
+            const uint32_t hv = pack_half2(p.centroids[e & 7] * ls, p.centroids[e >> 3] * ls);
+            const float ra = __low2float(*reinterpret_cast<const __half2*>(&hv));
+            const float rb = __high2float(*reinterpret_cast<const __half2*>(&hv));
+            const uint32_t n2 = __float_as_uint(ra * ra + rb * rb);  // as the MMA sees the pair
+            reinterpret_cast<uint4*>(smem)[i] = make_uint4(hv, n2, hv, n2);
+        }
+    } else if constexpr (KB == 4) {
+        // 256 entries x 32 lanes x 4 bytes; one 16-byte store writes four lanes' copies
+        for (int i = threadIdx.x; i < 256 * 8; i += NT) {
+            const int e = i >> 3;
+            const uint32_t hv = pack_half2(p.centroids[e & 15] * ls, p.centroids[e >> 4] * ls);
+            reinterpret_cast<uint4*>(smem)[i] = make_uint4(hv, hv, hv, hv);
+        }
+    }
+
+    // ---- queries: q' = Pi q (MSE keys), scaled, into B fragments ---------------
+    {
+        float* qs = reinterpret_cast<float*>(ring);
+        const uint16_t* qg = a.q + static_cast<int64_t>(s) * Hq * D;
+        for (int i = threadIdx.x; i < Hq * D; i += NT) {
+            float x = __uint_as_float(static_cast<uint32_t>(qg[i]) << 16);
+            if constexpr (KB != 8) {
+                const int dim = i % D;
+                if ((p.sign_mask[dim >> 5] >> (dim & 31)) & 1u) x = -x;
+            }
+            qs[i] = x;
+        }
+        if constexpr (KB != 8) {
+#pragma unroll 1
+            for (int st = 1; st < D; st <<= 1) {
+                __syncthreads();
+                for (int b = threadIdx.x; b < Hq * D / 2; b += NT) {
+                    const int row = b / (D / 2);
+                    const int j = b % (D / 2);
+                    const int i = (j / st) * 2 * st + (j % st);
+                    float* rw = qs + row * D;
+                    const float x0 = rw[i], x1 = rw[i + st];
+                    rw[i] = x0 + x1;
+                    rw[i + st] = x0 - x1;
+                }
+            }
+        }
+        __syncthreads();
+        // Scores come out in log2 units.  MSE keys: the table holds
+        // c * lut_scale and Pi carries 1/sqrt(d); without NC the table scale
+        // is divided out here (with NC it cancels in c / ||c||).
+        float f = a.qscale;
+        if constexpr (KB != 8) f *= rsqrtf(static_cast<float>(D)) * (NC ? 1.0f : 1.0f / ls);
+        const float* qrow = qs + (h * Gq + r) * D;
+        // fragments of this warp: [k-step][query row r < G][lane c]
+        uint4* dst = reinterpret_cast<uint4*>(smem + G::q_off(Hq)) + warp * G::KSTEPS * Gq * 4;
+        if (threadIdx.x == 0) *reinterpret_cast<uint4*>(smem + G::ZERO_OFF) = make_uint4(0u, 0u, 0u, 0u);
+        for (int jl = 0; jl < G::KSTEPS && r < Gq; ++jl) {
+            const int j = part * G::KSTEPS + jl;  // k-step of the whole head
+            const int u = cc * (D / 8) + 2 * j;   // pair index of b0; b1 is u + 1
+            const float x0 = qrow[2 * u] * f, x1 = qrow[2 * u + 1] * f;
+            const float x2 = qrow[2 * u + 2] * f, x3 = qrow[2 * u + 3] * f;
+            const uint32_t hi0 = pack_half2(x0, x1);
+            const uint32_t hi1 = pack_half2(x2, x3);
+            const __half2 h0 = *reinterpret_cast<const __half2*>(&hi0);
+            const __half2 h1 = *reinterpret_cast<const __half2*>(&hi1);
+            const uint32_t lo0 = pack_half2(x0 - __low2float(h0), x1 - __high2float(h0));
+            const uint32_t lo1 = pack_half2(x2 - __low2float(h1), x3 - __high2float(h1));
+            dst[(jl * Gq + r) * 4 + cc] = make_uint4(hi0, hi1, lo0, lo1);
+        }
+        __syncthreads();
+    }
+    // lanes of padded query rows (r >= G) read the zero block at every k-step
+    const bool q_real = r < Gq;
+    const uint4* qfrag = q_real ? reinterpret_cast<const uint4*>(smem + G::q_off(Hq)) + warp * G::KSTEPS * Gq * 4 +
+                                      r * 4 + cc
+                                : reinterpret_cast<const uint4*>(smem + G::ZERO_OFF);
+    const int qstride = q_real ? Gq * 4 : 0;
+
+    // ---- chunk staging: chunks are issued in order, so the (block, chunk in
+    // block) position advances by one per issue without any division ---------
+    const int cpb = c.block_size / kTok;  // 16-token chunks per paged block
+    int nxt_blk = c0 / cpb;               // block-table column of the next chunk to issue
+    int nxt_in = c0 - nxt_blk * cpb;      // its chunk index inside that block
+    const int32_t* bt_row = a.block_table + static_cast<int64_t>(s) * a.max_blocks;
+    auto issue_next = [&](int slot) -> int {
+        int b = bt_row[nxt_blk];
+        b = (b >= 0 && b < c.num_blocks) ? b : -1;
+        if (b >= 0) {
+            const uint8_t* src = c.data + static_cast<int64_t>(b) * c.block_stride +
+                                 static_cast<int64_t>(nxt_in) * G::CHUNK;
+            const uint32_t dst = ring_sh + slot * G::STAGE;
+            constexpr int kPieces = G::CHUNK / 16;
+#pragma unroll
+            for (int k = 0; k < (kPieces + NT - 1) / NT; ++k) {
+                const int i = static_cast<int>(threadIdx.x) + k * NT;
+                if (kPieces % NT == 0 || i < kPieces) cp_async16(dst + 16 * i, src + 16 * i);
+            }
+        }
+        if (++nxt_in == cpb) {
+            nxt_in = 0;
+            ++nxt_blk;
+        }
+        return b;
+    };
+
+    // ---- per-thread constant offsets inside a stage ---------------------------------
+    const int hs = h * SA;
+    const int k_off = r * ROW + hs + cc * G::KBYTES + part * G::KBYTES_W;  // token r; +8 ROW for r+8
+    const int n_off = r * ROW + hs + S::kKeyIdxBytes;                     // vec_norm of token r
+    const int z_off = r * ROW + hs + S::kKeyBytes + S::kValCodeBytes;     // scale, zero of token r
+    const int v_off = 2 * cc * ROW + hs + S::kKeyBytes + (r * (D / 8) * VB + part * G::VBITS_W) / 8;
+    const uint8_t* lut = smem;
+    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
+    const uint32_t lane8 = static_cast<uint32_t>(lane) << 3;
+
+    // ---- running state ---------------------------------------------------------------
+    float o[G::MTILES][4];
+#pragma unroll
+    for (int mt = 0; mt < G::MTILES; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+    float ob[4] = {0.f, 0.f, 0.f, 0.f};  // row 0: sum of P' per query column
+    float m_ref[2] = {-INFINITY, -INFINITY};
+    float l_acc[2] = {0.f, 0.f};
+    float z_acc[2] = {0.f, 0.f};
+    const uint32_t bias_a = (r == 0) ? 0x3C003C00u : 0u;
+    const uint32_t a_bias[4] = {bias_a, 0u, bias_a, 0u};
+    float* xch = reinterpret_cast<float*>(smem + G::X_OFF);  // [warp][lane][8]
+
+    const int nch = c1 - c0;
+    int bid[NS];
+#pragma unroll
+    for (int st = 0; st < NS; ++st) bid[st] = -1;
+#pragma unroll
+    for (int st = 0; st < NS - 1; ++st) {
+        if (st < nch) bid[st] = issue_next(st);
+        cp_async_commit();
+    }
+
+#pragma unroll 1
+    for (int base = 0; base < nch; base += NS) {
+#pragma unroll
+        for (int sl = 0; sl < NS; ++sl) {
+            const int it = base + sl;
+            if (it >= nch) break;
+            cp_async_wait<NS - 2>();
+            __syncthreads();
+            {
+                const int nslot = (sl + NS - 1) % NS;  // static once the loop is unrolled
+                if (it + NS - 1 < nch) bid[nslot] = issue_next(nslot);
+                cp_async_commit();
+            }
+            if (bid[sl] < 0) {
+                if (lane == 0 && warp == 0) set_flag(c.flags, kFlagBlock);
+                continue;
+            }
+            const int tok0 = (c0 + it) * kTok;
+            const uint8_t* stage = ring + sl * G::STAGE;
+            const bool v_r = tok0 + r < L;
+            const bool v_r8 = tok0 + r + 8 < L;
+
+            // ---- QK over this warp's share of the dims ------------------------------
+            // independent accumulators (even/odd k-step x hi/lo query part) keep
+            // the dependent-MMA chains short; summed after the loop
+            float qacc[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) qacc[i][e] = 0.f;
+            float nsq[2] = {0.f, 0.f};
+            float nacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                uint32_t kw0[G::KWORDS], kw1[G::KWORDS];
+                ld_words(stage + k_off, kw0);
+                ld_words(stage + k_off + 8 * ROW, kw1);
+#pragma unroll
+                for (int j = 0; j < G::KSTEPS; ++j) {
+                    uint32_t af[4];
+                    if constexpr (KB == 3) {
+                        // local pairs 2j (a0/a1) and 2j+1 (a2/a3): 6-bit fields at bit 6 * pair
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int bit = 6 * (2 * j + e);
+                            const int wi = bit / 32, off = bit % 32;
+                            uint32_t x0, x1;
+                            if (off + 6 <= 32) {
+                                x0 = off <= 8 ? (kw0[wi] << (8 - off)) : (kw0[wi] >> (off - 8));
+                                x1 = off <= 8 ? (kw1[wi] << (8 - off)) : (kw1[wi] >> (off - 8));
+                            } else {
+                                x0 = __funnelshift_r(kw0[wi], kw0[wi + 1], off - 8);
+                                x1 = __funnelshift_r(kw1[wi], kw1[wi + 1], off - 8);
+                            }
+                            const uint2 t0 = *reinterpret_cast<const uint2*>(lut + ((x0 & 0x3F00u) | lane8));
+                            const uint2 t1 = *reinterpret_cast<const uint2*>(lut + ((x1 & 0x3F00u) | lane8));
+                            af[2 * e] = t0.x;
+                            af[2 * e + 1] = t1.x;
+                            if constexpr (NC) {
+                                nsq[0] += __uint_as_float(t0.y);
+                                nsq[1] += __uint_as_float(t1.y);
+                            }
+                        }
+                    } else if constexpr (KB == 4) {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int bit = 8 * (2 * j + e);
+                            const int wi = bit / 32, off = bit % 32;
+                            const uint32_t x0 = off <= 7 ? (kw0[wi] << (7 - off)) : (kw0[wi] >> (off - 7));
+                            const uint32_t x1 = off <= 7 ? (kw1[wi] << (7 - off)) : (kw1[wi] >> (off - 7));
+                            af[2 * e] = ld32(lut + ((x0 & 0x7F80u) | lane4));
+                            af[2 * e + 1] = ld32(lut + ((x1 & 0x7F80u) | lane4));
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int bit = 16 * (2 * j + e);
+                            const int wi = bit / 32, off = bit % 32;
+                            const __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
+                                static_cast<__nv_fp8x2_storage_t>((kw0[wi] >> off) & 0xffffu), __NV_E4M3);
+                            const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(
+                                static_cast<__nv_fp8x2_storage_t>((kw1[wi] >> off) & 0xffffu), __NV_E4M3);
+                            af[2 * e] = static_cast<uint32_t>(h0.x) | (static_cast<uint32_t>(h0.y) << 16);
+                            af[2 * e + 1] = static_cast<uint32_t>(h1.x) | (static_cast<uint32_t>(h1.y) << 16);
+                        }
+                    }
+                    // af = {tok r pair 2j, tok r+8 pair 2j, tok r pair 2j+1, tok r+8 pair 2j+1}
+                    const uint32_t afrag[4] = {af[0], af[1], af[2], af[3]};
+                    const uint4 qb = qfrag[j * qstride];
+                    mma16816(qacc[2 * (j & 1)], afrag, qb.x, qb.y);
+                    mma16816(qacc[2 * (j & 1) + 1], afrag, qb.z, qb.w);
+                    if constexpr (NC && KB == 4) {
+                        uint32_t sq[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __half2 x = *reinterpret_cast<const __half2*>(&afrag[e]);
+                            const __half2 y = __hmul2(x, x);
+                            sq[e] = *reinterpret_cast<const uint32_t*>(&y);
+                        }
+                        mma16816(nacc[j & 1], sq, 0x3C003C00u, 0x3C003C00u);  // every column: sum of squares
+                    }
+                }
+            }
+            float sacc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[e] = (qacc[0][e] + qacc[2][e]) + (qacc[1][e] + qacc[3][e]);
+            float n0 = 0.f, n1 = 0.f;  // ||c~||^2 of tokens r, r + 8 (this warp's share)
+            if constexpr (NC && KB == 3) {
+                n0 = nsq[0] + __shfl_xor_sync(kFull, nsq[0], 1);
+                n0 += __shfl_xor_sync(kFull, n0, 2);
+                n1 = nsq[1] + __shfl_xor_sync(kFull, nsq[1], 1);
+                n1 += __shfl_xor_sync(kFull, n1, 2);
+            } else if constexpr (NC && KB == 4) {
+                n0 = nacc[0][0] + nacc[1][0];
+                n1 = nacc[0][2] + nacc[1][2];
+            }
+            if constexpr (WPH > 1) {
+                // add the other warps' shares of the dims
+                float4* mine = reinterpret_cast<float4*>(xch + (warp * 32 + lane) * 8);
+                mine[0] = make_float4(sacc[0], sacc[1], sacc[2], sacc[3]);
+                mine[1] = make_float4(n0, n1, 0.f, 0.f);
+                group_barrier(1 + h, 32 * WPH);
+#pragma unroll
+                for (int w = 1; w < WPH; ++w) {
+                    const int ow = h * WPH + (part + w) % WPH;
+                    const float4* other = reinterpret_cast<const float4*>(xch + (ow * 32 + lane) * 8);
+                    const float4 os = other[0];
+                    const float4 on = other[1];
+                    sacc[0] += os.x;
+                    sacc[1] += os.y;
+                    sacc[2] += os.z;
+                    sacc[3] += os.w;
+                    n0 += on.x;
+                    n1 += on.y;
+                }
+            }
+
+            // ---- per-token factors: vec_norm, norm correction, masking -------------
+            float f_r = 1.f, f_r8 = 1.f;
+            if constexpr (KB != 8) {
+                f_r = half_from_bits(ld16(stage + n_off));
+                f_r8 = half_from_bits(ld16(stage + n_off + 8 * ROW));
+                if constexpr (NC) {
+                    f_r *= rsqrtf(n0);
+                    f_r8 *= rsqrtf(n1);
+                }
+            }
+            float sc[4];
+            sc[0] = v_r ? sacc[0] * f_r : -INFINITY;
+            sc[1] = v_r ? sacc[1] * f_r : -INFINITY;
+            sc[2] = v_r8 ? sacc[2] * f_r8 : -INFINITY;
+            sc[3] = v_r8 ? sacc[3] * f_r8 : -INFINITY;
+
+            // ---- online softmax (log2 domain), lazy rescale ---------------------------
+            float mx0 = fmaxf(sc[0], sc[2]);
+            float mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+            for (int m = 4; m < 32; m <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, m));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, m));
+            }
+            const bool grow = (mx0 > m_ref[0] + kRescaleThreshold) || (mx1 > m_ref[1] + kRescaleThreshold);
+            if (__any_sync(kFull, grow)) {
+                const float n0m = fmaxf(m_ref[0], mx0);
+                const float n1m = fmaxf(m_ref[1], mx1);
+                const float al0 = (n0m == -INFINITY) ? 1.f : fast_exp2(m_ref[0] - n0m);
+                const float al1 = (n1m == -INFINITY) ? 1.f : fast_exp2(m_ref[1] - n1m);
+#pragma unroll
+                for (int mt = 0; mt < G::MTILES; ++mt) {
+                    o[mt][0] *= al0;
+                    o[mt][1] *= al1;
+                    o[mt][2] *= al0;
+                    o[mt][3] *= al1;
+                }
+                ob[0] *= al0;
+                ob[1] *= al1;
+                ob[2] *= al0;
+                ob[3] *= al1;
+                l_acc[0] *= al0;
+                l_acc[1] *= al1;
+                z_acc[0] *= al0;
+                z_acc[1] *= al1;
+                m_ref[0] = n0m;
+                m_ref[1] = n1m;
+            }
+            float pr[4];
+            pr[0] = (sc[0] == -INFINITY) ? 0.f : fast_exp2(sc[0] - m_ref[0]);
+            pr[1] = (sc[1] == -INFINITY) ? 0.f : fast_exp2(sc[1] - m_ref[1]);
+            pr[2] = (sc[2] == -INFINITY) ? 0.f : fast_exp2(sc[2] - m_ref[0]);
+            pr[3] = (sc[3] == -INFINITY) ? 0.f : fast_exp2(sc[3] - m_ref[1]);
+            l_acc[0] += pr[0] + pr[2];
+            l_acc[1] += pr[1] + pr[3];
+
+            // value scale / zero of tokens r and r + 8
+            float vs_r = 0.f, vz_r = 0.f, vs_r8 = 0.f, vz_r8 = 0.f;
+            {
+                const uint32_t sz0 = static_cast<uint32_t>(ld16(stage + z_off)) |
+                                     (static_cast<uint32_t>(ld16(stage + z_off + 2)) << 16);
+                const uint32_t sz1 = static_cast<uint32_t>(ld16(stage + z_off + 8 * ROW)) |
+                                     (static_cast<uint32_t>(ld16(stage + z_off + 8 * ROW + 2)) << 16);
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&sz0));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&sz1));
+                if (v_r) {
+                    vs_r = f0.x;
+                    vz_r = f0.y;
+                }
+                if (v_r8) {
+                    vs_r8 = f1.x;
+                    vz_r8 = f1.y;
+                }
+            }
+            // zero point plus the centre of the code range (codes enter centred)
+            const float zc_r = vz_r + kCentre * vs_r;
+            const float zc_r8 = vz_r8 + kCentre * vs_r8;
+            z_acc[0] += pr[0] * zc_r + pr[2] * zc_r8;
+            z_acc[1] += pr[1] * zc_r + pr[3] * zc_r8;
+            const uint32_t pb0 = movmatrix_trans(pack_half2(pr[0] * vs_r, pr[1] * vs_r));
+            const uint32_t pb1 = movmatrix_trans(pack_half2(pr[2] * vs_r8, pr[3] * vs_r8));
+
+            // ---- P.V over this warp's share of the dims --------------------------------
+            {
+                uint32_t w0[G::VWORDS], w1[G::VWORDS], w8[G::VWORDS], w9[G::VWORDS];
+                ld_words(stage + v_off, w0);
+                ld_words(stage + v_off + ROW, w1);
+                ld_words(stage + v_off + 8 * ROW, w8);
+                ld_words(stage + v_off + 9 * ROW, w9);
+#pragma unroll
+                for (int mt = 0; mt < G::MTILES; ++mt) {
+                    uint32_t vf[4];
+                    vf[0] = value_pair<VB>(w0, w1, 2 * mt);
+                    vf[1] = value_pair<VB>(w0, w1, 2 * mt + 1);
+                    vf[2] = value_pair<VB>(w8, w9, 2 * mt);
+                    vf[3] = value_pair<VB>(w8, w9, 2 * mt + 1);
+                    mma16816(o[mt], vf, pb0, pb1);
+                }
+                mma16816(ob, a_bias, pb0, pb1);
+            }
+        }
+    }
+    cp_async_wait<0>();
+
+    // ---- partial state ------------------------------------------------------------------
+#pragma unroll
+    for (int m = 4; m < 32; m <<= 1) {
+        l_acc[0] += __shfl_xor_sync(kFull, l_acc[0], m);
+        l_acc[1] += __shfl_xor_sync(kFull, l_acc[1], m);
+        z_acc[0] += __shfl_xor_sync(kFull, z_acc[0], m);
+        z_acc[1] += __shfl_xor_sync(kFull, z_acc[1], m);
+    }
+    const float bias0 = __shfl_sync(kFull, ob[0], cc);
+    const float bias1 = __shfl_sync(kFull, ob[1], cc);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int q = 2 * cc + e;
+        if (q >= Gq) continue;
+        const int hq = h * Gq + q;
+        float* part_out = a.partials + ((static_cast<int64_t>(s) * Hq + hq) * a.num_splits + split) * (D + 2);
+        if (r == 0 && part == 0) {
+            part_out[0] = m_ref[e];
+            part_out[1] = l_acc[e];
+        }
+        const float bias = e ? bias1 : bias0;
+        const float z = z_acc[e];
+#pragma unroll
+        for (int mt = 0; mt < G::MTILES; ++mt) {
+            // sum P'(code - centre) = 2^VB (o - bias) - centre * bias
+            const int d0 = r * (D / 8) + 2 * (part * G::MTILES + mt);
+            part_out[2 + d0] = (o[mt][e] - bias) * kValW - kCentre * bias + z;
+            part_out[2 + d0 + 1] = (o[mt][2 + e] - bias) * kValW - kCentre * bias + z;
+        }
+    }
+}
+
+template <int D, int KB, int VB>
+constexpr bool share_aligned(int wph) {
+    // each warp's share of a thread's key and value codes starts on a byte
+    return ((D / 4 / wph) * KB) % 8 == 0 && ((D / 8 / wph) * VB) % 8 == 0 && (D / 16) % wph == 0;
+}
+
+template <int D, int KB, int VB>
+constexpr int pick_wph(int want) {
+    int w = want;
+    while (w > 1 && !share_aligned<D, KB, VB>(w)) w /= 2;
+    return w;
+}
+
+// Launch policy per shape: warps per head, resident CTAs per SM aimed for,
+// and the deepest stage ring that fits the shared memory that leaves.
+template <int D, int KB, int VB, int H>
+struct Policy {
+    static constexpr int kWarpsTarget = 8;
+    static constexpr int kWphRaw = kWarpsTarget / H;
+    static constexpr int kWphMax = D / 32;  // at least two k-steps per warp
+    static constexpr int WPH = pick_wph<D, KB, VB>(kWphRaw < 1 ? 1 : (kWphRaw > kWphMax ? kWphMax : kWphRaw));
+    static constexpr int MINB = 32 * H * WPH > 256 ? 1 : 2;
+    static constexpr int kBudget = MINB == 1 ? 220 * 1024 : 110 * 1024;
+    using G1 = Geo<D, KB, VB, H, WPH, 1>;
+    // fixed part plus the query fragments of up to 5 query heads per KV head
+    static constexpr int kFixed = G1::RING_OFF + 16 + H * 5 * D * 4;
+    static constexpr int kNs = (kBudget - kFixed) / G1::STAGE;
+    static constexpr int NS = kNs < 2 ? 2 : (kNs > 8 ? 8 : kNs);
+};
+
+template <int D, int KB, int VB, bool NC, int H>
+struct Kernel {
+    using P = Policy<D, KB, VB, H>;
+    using G = Geo<D, KB, VB, H, P::WPH, P::NS>;
+    static constexpr auto fn = decode_kernel<D, KB, VB, NC, H, P::WPH, P::NS, P::MINB>;
+
+    static cudaError_t prepare(int hq, int* smem) {
+        *smem = G::smem_bytes(hq);
+        return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, *smem);
+    }
+    static cudaError_t occupancy(int hq, int* ctas) {
+        int smem = 0;
+        const cudaError_t e = prepare(hq, &smem);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, fn, G::NT, smem);
+    }
+    static cudaError_t launch(const LayerParams& p, const CacheGeom& c, const Args& a, int num_seqs,
+                              cudaStream_t stream) {
+        int smem = 0;
+        const cudaError_t e = prepare(a.num_q_heads, &smem);
+        if (e != cudaSuccess) return e;
+        dim3 grid(static_cast<unsigned>(a.num_splits), static_cast<unsigned>(num_seqs));
+        fn<<<grid, G::NT, smem, stream>>>(p, c, a);
+        return cudaGetLastError();
+    }
+};
+
+// One entry per head size: occupancy query (ctas != nullptr) or launch.
+template <int D>
+cudaError_t run(const LayerParams& p, const CacheGeom& c, const Args& a, int num_seqs, int num_kv_heads,
+                cudaStream_t stream, int* ctas) {
+    auto go = [&](auto kern) -> cudaError_t {
+        using K = decltype(kern);
+        if (ctas != nullptr) return K::occupancy(a.num_q_heads, ctas);
+        return K::launch(p, c, a, num_seqs, stream);
+    };
+    auto by_h = [&](auto kb, auto vb, auto nc) -> cudaError_t {
+        constexpr int KB = decltype(kb)::value, VB = decltype(vb)::value;
+        constexpr bool NC = decltype(nc)::value;
+        switch (num_kv_heads) {
+            case 1: return go(Kernel<D, KB, VB, NC, 1>{});
+            case 2: return go(Kernel<D, KB, VB, NC, 2>{});
+            case 4: return go(Kernel<D, KB, VB, NC, 4>{});
+            case 8: return go(Kernel<D, KB, VB, NC, 8>{});
+            default: return cudaErrorInvalidValue;
+        }
+    };
+    auto by_nc = [&](auto kb, auto vb) -> cudaError_t {
+        if constexpr (decltype(kb)::value != 8) {
+            if (p.nc) return by_h(kb, vb, std::true_type{});
+        }
+        return by_h(kb, vb, std::false_type{});
+    };
+    using I3 = std::integral_constant<int, 3>;
+    using I4 = std::integral_constant<int, 4>;
+    using I8 = std::integral_constant<int, 8>;
+    const int kb = p.kbits, vb = p.vbits;
+    if (kb == 3 && vb == 3) return by_nc(I3{}, I3{});
+    if (kb == 3 && vb == 4) return by_nc(I3{}, I4{});
+    if (kb == 4 && vb == 3) return by_nc(I4{}, I3{});
+    if (kb == 4 && vb == 4) return by_nc(I4{}, I4{});
+    if (kb == 8 && vb == 3) return by_nc(I8{}, I3{});
+    if (kb == 8 && vb == 4) return by_nc(I8{}, I4{});
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace mma
+}  // namespace tq
+
+namespace tq {
+// One translation unit per head size (tq_decode_mma_d{64,128,256}.cu).
+// ctas != nullptr: report resident CTAs per SM instead of launching.
+cudaError_t decode_mma_run_d64(const LayerParams& p, const CacheGeom& c, const mma::Args& a, int num_seqs,
+                               int num_kv_heads, cudaStream_t stream, int* ctas);
+cudaError_t decode_mma_run_d128(const LayerParams& p, const CacheGeom& c, const mma::Args& a, int num_seqs,
+                                int num_kv_heads, cudaStream_t stream, int* ctas);
+cudaError_t decode_mma_run_d256(const LayerParams& p, const CacheGeom& c, const mma::Args& a, int num_seqs,
+                                int num_kv_heads, cudaStream_t stream, int* ctas);
+}  // namespace tq

@@ -62,6 +62,8 @@ cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16
 
 // Tensor-core decode (tq_decode_mma.cu): H in {1,2,4,8}, G <= 8, d in {64,128,256}.
 bool decode_mma_supported(const LayerParams& p, int num_kv_heads, int num_q_heads);
+// Resident CTAs per SM of the tensor-core decode for these shapes (0 on error).
+int decode_mma_ctas_per_sm(const LayerParams& p, int num_kv_heads, int num_q_heads);
 cudaError_t launch_decode_mma(const LayerParams& p, const CacheGeom& c, const uint16_t* q, int num_seqs,
                               int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
                               const int32_t* seq_lens, int max_seq_len, float sm_scale, const DecodePlan& plan,
