@@ -68,6 +68,8 @@ typedef enum tq_status {
 #define TQ_FLAG_SLOT_OUT_OF_RANGE  1u  /* slot_mapping[t] >= num_blocks * block_size */
 #define TQ_FLAG_BLOCK_OUT_OF_RANGE 2u  /* block_table entry < 0 or >= num_blocks */
 #define TQ_FLAG_SEQ_TOO_LONG       4u  /* seq_len > max_blocks_per_seq * block_size or > max_seq_len */
+#define TQ_FLAG_WAIT_TIMEOUT       8u  /* a decode kernel gave up waiting (about 1 s) for a staged
+                                          chunk; that call's outputs are not valid */
 
 /*
  * Quantiser configuration: [TQC] TurboQuantConfig fields plus every derived

@@ -31,6 +31,7 @@ TQ_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # include/tq.h
 TQ_FLAG_SLOT_OUT_OF_RANGE = 1
 TQ_FLAG_BLOCK_OUT_OF_RANGE = 2
 TQ_FLAG_SEQ_TOO_LONG = 4
+TQ_FLAG_WAIT_TIMEOUT = 8
 
 _PKG = Path(__file__).resolve().parent
 

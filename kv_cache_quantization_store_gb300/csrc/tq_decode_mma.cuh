@@ -69,12 +69,47 @@ struct Args {
     float lut_scale;  // table value = centroid * lut_scale (= gamma * sqrt(d))
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr), "l"(gmem));
+// One-dimensional bulk copy global -> shared that signals completion on an
+// mbarrier of this CTA (complete_tx of `bytes`).
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(mbar)
+        : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(mbar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(mbar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for phase `parity` of an mbarrier, giving up after about a second.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+    if (mbar_try_wait(mbar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(mbar, parity))
+        if (clock64() - t0 > (1ll << 31)) return false;
+    return true;
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+// Shared-memory counter increment with acquire-release ordering; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t addr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -131,34 +166,40 @@ __device__ __forceinline__ void ld_words(const uint8_t* p, uint32_t (&w)[NW]) {
     for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
 }
 
-// Value codes of local dim n for two tokens as f16x2: 1 + code / 2^VB,
-// tokens a in the low half and b in the high half.
+// Value code of local dim n for two tokens as an fp16 subnormal pair
+// (token a in the low half, token b in the high half): the code's bits are
+// masked in place inside a 16-bit window that starts on the byte holding the
+// code's first bit, so the half is code * 2^(pos - 24) with pos = (n VB) mod 8
+// (pos + VB <= 10: the field never reaches the exponent bits).
 template <int VB, int NW>
-__device__ __forceinline__ uint32_t value_pair(const uint32_t (&wa)[NW], const uint32_t (&wb)[NW], int n) {
-    constexpr int kPlace = 10 - VB;  // code lands in mantissa bits [kPlace, 10)
-    constexpr uint32_t kMask = ((1u << VB) - 1u) << kPlace;
+__device__ __forceinline__ uint32_t value_sub(const uint32_t (&wa)[NW], const uint32_t (&wb)[NW], int n) {
     const int bit = n * VB;
-    int b0;  // first byte of a 16-bit window that holds the field
-    if ((bit % 16) + VB <= 16) b0 = 2 * (bit / 16);
-    else b0 = bit / 8;
+    const int b0 = bit / 8, pos = bit % 8;
+    const int w = b0 / 4, o = b0 % 4;
     uint32_t win;
-    if (b0 % 4 <= 2) {
-        const int o = b0 % 4;
-        const uint32_t sel = o | ((o + 1) << 4) | ((o + 4) << 8) | ((o + 5) << 12);
-        win = prmt(wa[b0 / 4], wb[b0 / 4], sel);
+    if (o <= 2) {
+        // bytes b0, b0 + 1 of both tokens (one selector per byte, shared by its codes)
+        win = prmt(wa[w], wb[w], o | ((o + 1) << 4) | ((o + 4) << 8) | ((o + 5) << 12));
+    } else if (pos + VB <= 8) {
+        win = prmt(wa[w], wb[w], 3 | (3 << 4) | (7 << 8) | (7 << 12));
     } else {
-        const uint32_t fa = __funnelshift_r(wa[b0 / 4], wa[b0 / 4 + 1], 24);
-        const uint32_t fb = __funnelshift_r(wb[b0 / 4], wb[b0 / 4 + 1], 24);
+        const uint32_t fa = __funnelshift_r(wa[w], wa[w + 1], 24);
+        const uint32_t fb = __funnelshift_r(wb[w], wb[w + 1], 24);
         win = prmt(fa, fb, 0x5410);
     }
-    const int pos = bit - 8 * b0;  // field position inside each 16-bit half
-    const int sh = kPlace - pos;
-    const uint32_t x = sh >= 0 ? (win << sh) : (win >> (-sh));
-    return (x & (kMask | (kMask << 16))) | 0x3C003C00u;
+    constexpr uint32_t kField = (1u << VB) - 1u;
+    return win & ((kField << pos) * 0x00010001u);
+}
+
+// 2^(24 - pos): turns the accumulated subnormal products of local dim n back
+// into code units.
+template <int VB>
+__device__ __forceinline__ constexpr float value_weight(int n) {
+    return static_cast<float>(1u << (24 - (n * VB) % 8));
 }
 
 // Compile-time geometry of one kernel instantiation.  Shared memory:
-// [pair table][score exchange][16 zero bytes][stage ring][Q' fragments].
+// [pair table][score exchange x2][control][16 zero bytes][stage ring][Q' fragments].
 template <int D, int KB, int VB, int H, int WPH, int NS>
 struct Geo {
     using S = Slot<D, KB, VB>;
@@ -178,9 +219,12 @@ struct Geo {
     static constexpr int LUT_ENTRY = KB == 3 ? 8 : 4;
     static constexpr int LUT_ENTRIES = KB == 3 ? 64 : (KB == 4 ? 256 : 0);
     static constexpr int LUT_BYTES = LUT_ENTRIES * 32 * LUT_ENTRY;
-    static constexpr int XCH_W = WPH > 1 ? 32 * 8 * 4 : 0;
+    static constexpr int XCH_W = WPH > 1 ? 32 * 8 * 4 : 0;  // per warp and buffer
     static constexpr int X_OFF = LUT_BYTES;
-    static constexpr int ZERO_OFF = X_OFF + NWARPS * XCH_W;
+    // control block: full mbarrier, release counter, block id per stage; error word
+    static constexpr int CTRL_OFF = X_OFF + 2 * NWARPS * XCH_W;
+    static constexpr int CTRL_BYTES = (16 * NS + 16 + 15) & ~15;
+    static constexpr int ZERO_OFF = CTRL_OFF + CTRL_BYTES;
     static constexpr int RING_OFF = ZERO_OFF + 16;
     static constexpr int RING = NS * STAGE + 16;
     // Q' fragments follow the ring: per warp, k-step and query row r < G,
@@ -202,7 +246,6 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     constexpr int SA = G::SA;
     constexpr int ROW = G::ROW;
     constexpr int NT = G::NT;
-    constexpr float kValW = static_cast<float>(1 << VB);  // 1 / weight of a code in the fp16 operand
     constexpr float kCentre = 0.5f * static_cast<float>((1 << VB) - 1);
     extern __shared__ __align__(16) uint8_t smem[];
 
@@ -229,6 +272,18 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     const int n_chunks = (L + kTok - 1) / kTok;
     const int c0 = split * a.chunks_per_split;
     const int c1 = min(c0 + a.chunks_per_split, n_chunks);
+
+    // ---- control block: stage mbarriers and counters ------------------------------
+    if (threadIdx.x == 0) {
+        uint8_t* ctl = smem + G::CTRL_OFF;
+        const uint32_t ctl_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ctl));
+        for (int st = 0; st < NS; ++st) {
+            mbar_init(ctl_sh + 8u * st, 1u);
+            reinterpret_cast<uint32_t*>(ctl + 8 * NS)[st] = 0u;
+            reinterpret_cast<int*>(ctl + 12 * NS)[st] = -1;
+        }
+        *reinterpret_cast<int*>(ctl + 16 * NS) = 0;
+    }
 
     // ---- pair lookup table: centroids * lut_scale as fp16, one copy per lane ----
     const float ls = a.lut_scale;
@@ -310,32 +365,40 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
                                 : reinterpret_cast<const uint4*>(smem + G::ZERO_OFF);
     const int qstride = q_real ? Gq * 4 : 0;
 
-    // ---- chunk staging: chunks are issued in order, so the (block, chunk in
-    // block) position advances by one per issue without any division ---------
+    // ---- chunk staging.  Chunk it (of this split) lives in stage it % NS; one
+    // thread copies all of it (16 token rows of every head, contiguous in the
+    // paged block) with one bulk copy that completes the stage's mbarrier.  A
+    // warp releases a stage once its data is in registers; the last warp to
+    // release it refills it with chunk it + NS.  No CTA-wide barrier in the loop.
+    uint8_t* const ctrl = smem + G::CTRL_OFF;
+    const uint32_t ctrl_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ctrl));
+    auto full_bar = [&](int slot) -> uint32_t { return ctrl_sh + 8u * slot; };
+    auto cnt_addr = [&](int slot) -> uint32_t { return ctrl_sh + 8u * NS + 4u * slot; };
+    int* const stage_blk = reinterpret_cast<int*>(ctrl + 12 * NS);  // block id of the staged chunk, -1: none
+    int* const err_word = reinterpret_cast<int*>(ctrl + 16 * NS);
     const int cpb = c.block_size / kTok;  // 16-token chunks per paged block
-    int nxt_blk = c0 / cpb;               // block-table column of the next chunk to issue
-    int nxt_in = c0 - nxt_blk * cpb;      // its chunk index inside that block
     const int32_t* bt_row = a.block_table + static_cast<int64_t>(s) * a.max_blocks;
-    auto issue_next = [&](int slot) -> int {
-        int b = bt_row[nxt_blk];
+    const int nch = c1 - c0;
+    auto issue = [&](int it) {  // one thread
+        const int slot = it % NS;
+        const int cg = c0 + it;
+        const int col = cg / cpb;
+        int b = bt_row[col];
         b = (b >= 0 && b < c.num_blocks) ? b : -1;
+        stage_blk[slot] = b;
         if (b >= 0) {
-            const uint8_t* src = c.data + static_cast<int64_t>(b) * c.block_stride +
-                                 static_cast<int64_t>(nxt_in) * G::CHUNK;
-            const uint32_t dst = ring_sh + slot * G::STAGE;
-            constexpr int kPieces = G::CHUNK / 16;
-#pragma unroll
-            for (int k = 0; k < (kPieces + NT - 1) / NT; ++k) {
-                const int i = static_cast<int>(threadIdx.x) + k * NT;
-                if (kPieces % NT == 0 || i < kPieces) cp_async16(dst + 16 * i, src + 16 * i);
-            }
+            const uint8_t* src =
+                c.data + static_cast<int64_t>(b) * c.block_stride + static_cast<int64_t>(cg - col * cpb) * G::CHUNK;
+            mbar_arrive_tx(full_bar(slot), G::CHUNK);
+            bulk_copy(ring_sh + slot * G::STAGE, src, G::CHUNK, full_bar(slot));
+        } else {
+            mbar_arrive(full_bar(slot));
         }
-        if (++nxt_in == cpb) {
-            nxt_in = 0;
-            ++nxt_blk;
-        }
-        return b;
     };
+    if (threadIdx.x == 0) {
+        fence_proxy_async();  // the ring held the query rotation (generic proxy writes)
+        for (int it = 0; it < NS && it < nch; ++it) issue(it);
+    }
 
     // ---- per-thread constant offsets inside a stage ---------------------------------
     const int hs = h * SA;
@@ -346,6 +409,153 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     const uint8_t* lut = smem;
     const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
     const uint32_t lane8 = static_cast<uint32_t>(lane) << 3;
+    float* xch = reinterpret_cast<float*>(smem + G::X_OFF);  // [buffer][warp][lane][8]
+
+    // ---- QK of one staged chunk: log2-domain scores of tokens r, r + 8 for
+    // query columns 2c, 2c + 1, -inf past the sequence end ---------------------------
+    auto qk = [&](const uint8_t* stage, int tok0, bool ok, int buf, float (&sc)[4]) {
+        float qacc[2][4];  // hi and lo query parts
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qacc[i][e] = 0.f;
+        float nsq[2] = {0.f, 0.f};
+        float nacc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t kw0[G::KWORDS], kw1[G::KWORDS];
+        ld_words(stage + k_off, kw0);
+        ld_words(stage + k_off + 8 * ROW, kw1);
+#pragma unroll
+        for (int j = 0; j < G::KSTEPS; ++j) {
+            // a = {tok r pair 2j, tok r+8 pair 2j, tok r pair 2j+1, tok r+8 pair 2j+1}
+            uint32_t af[4];
+            if constexpr (KB == 3) {
+                // 6-bit pair codes at bit 6 * pair; table entry {half2 c, float c0^2 + c1^2}
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int bit = 6 * (2 * j + e);
+                    const int wi = bit / 32, off = bit % 32;
+                    uint32_t x0, x1;
+                    if (off + 6 <= 32) {
+                        x0 = off <= 8 ? (kw0[wi] << (8 - off)) : (kw0[wi] >> (off - 8));
+                        x1 = off <= 8 ? (kw1[wi] << (8 - off)) : (kw1[wi] >> (off - 8));
+                    } else {
+                        x0 = __funnelshift_r(kw0[wi], kw0[wi + 1], off - 8);
+                        x1 = __funnelshift_r(kw1[wi], kw1[wi + 1], off - 8);
+                    }
+                    const uint2 t0 = *reinterpret_cast<const uint2*>(lut + ((x0 & 0x3F00u) | lane8));
+                    const uint2 t1 = *reinterpret_cast<const uint2*>(lut + ((x1 & 0x3F00u) | lane8));
+                    af[2 * e] = t0.x;
+                    af[2 * e + 1] = t1.x;
+                    if constexpr (NC) {
+                        nsq[0] += __uint_as_float(t0.y);
+                        nsq[1] += __uint_as_float(t1.y);
+                    }
+                }
+            } else if constexpr (KB == 4) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int bit = 8 * (2 * j + e);
+                    const int wi = bit / 32, off = bit % 32;
+                    const uint32_t x0 = off <= 7 ? (kw0[wi] << (7 - off)) : (kw0[wi] >> (off - 7));
+                    const uint32_t x1 = off <= 7 ? (kw1[wi] << (7 - off)) : (kw1[wi] >> (off - 7));
+                    af[2 * e] = ld32(lut + ((x0 & 0x7F80u) | lane4));
+                    af[2 * e + 1] = ld32(lut + ((x1 & 0x7F80u) | lane4));
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int bit = 16 * (2 * j + e);
+                    const int wi = bit / 32, off = bit % 32;
+                    const __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
+                        static_cast<__nv_fp8x2_storage_t>((kw0[wi] >> off) & 0xffffu), __NV_E4M3);
+                    const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(
+                        static_cast<__nv_fp8x2_storage_t>((kw1[wi] >> off) & 0xffffu), __NV_E4M3);
+                    af[2 * e] = static_cast<uint32_t>(h0.x) | (static_cast<uint32_t>(h0.y) << 16);
+                    af[2 * e + 1] = static_cast<uint32_t>(h1.x) | (static_cast<uint32_t>(h1.y) << 16);
+                }
+            }
+            const uint32_t afrag[4] = {af[0], af[1], af[2], af[3]};
+            const uint4 qb = qfrag[j * qstride];
+            mma16816(qacc[0], afrag, qb.x, qb.y);
+            mma16816(qacc[1], afrag, qb.z, qb.w);
+            if constexpr (NC && KB == 4) {
+                uint32_t sq[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __half2 x = *reinterpret_cast<const __half2*>(&afrag[e]);
+                    const __half2 y = __hmul2(x, x);
+                    sq[e] = *reinterpret_cast<const uint32_t*>(&y);
+                }
+                mma16816(nacc, sq, 0x3C003C00u, 0x3C003C00u);  // every column: sum of squares
+            }
+        }
+        float sacc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[e] = qacc[0][e] + qacc[1][e];
+        float n0 = 0.f, n1 = 0.f;  // ||c~||^2 of tokens r, r + 8 (this warp's share)
+        if constexpr (NC && KB == 3) {
+            n0 = nsq[0] + __shfl_xor_sync(kFull, nsq[0], 1);
+            n0 += __shfl_xor_sync(kFull, n0, 2);
+            n1 = nsq[1] + __shfl_xor_sync(kFull, nsq[1], 1);
+            n1 += __shfl_xor_sync(kFull, n1, 2);
+        } else if constexpr (NC && KB == 4) {
+            n0 = nacc[0];
+            n1 = nacc[2];
+        }
+        if constexpr (WPH > 1) {
+            // add the other warps' shares of the dims
+            float* xb = xch + buf * (G::NWARPS * 32 * 8);  // alternate buffers: no overwrite before it is read
+            float4* mine = reinterpret_cast<float4*>(xb + (warp * 32 + lane) * 8);
+            mine[0] = make_float4(sacc[0], sacc[1], sacc[2], sacc[3]);
+            mine[1] = make_float4(n0, n1, 0.f, 0.f);
+            group_barrier(1 + h, 32 * WPH);
+#pragma unroll
+            for (int w = 1; w < WPH; ++w) {
+                const int ow = h * WPH + (part + w) % WPH;
+                const float4* other = reinterpret_cast<const float4*>(xb + (ow * 32 + lane) * 8);
+                const float4 os = other[0];
+                const float4 on = other[1];
+                sacc[0] += os.x;
+                sacc[1] += os.y;
+                sacc[2] += os.z;
+                sacc[3] += os.w;
+                n0 += on.x;
+                n1 += on.y;
+            }
+        }
+        // per-token factors: vec_norm, norm correction
+        float f_r = 1.f, f_r8 = 1.f;
+        if constexpr (KB != 8) {
+            f_r = half_from_bits(ld16(stage + n_off));
+            f_r8 = half_from_bits(ld16(stage + n_off + 8 * ROW));
+            if constexpr (NC) {
+                f_r *= rsqrtf(n0);
+                f_r8 *= rsqrtf(n1);
+            }
+        }
+        const bool v_r = ok && tok0 + r < L;
+        const bool v_r8 = ok && tok0 + r + 8 < L;
+        sc[0] = v_r ? sacc[0] * f_r : -INFINITY;
+        sc[1] = v_r ? sacc[1] * f_r : -INFINITY;
+        sc[2] = v_r8 ? sacc[2] * f_r8 : -INFINITY;
+        sc[3] = v_r8 ? sacc[3] * f_r8 : -INFINITY;
+    };
+
+    // ---- value codes and (scale, zero) of one staged chunk, kept in registers
+    // until the chunk's P.V one step later ------------------------------------------
+    struct VRegs {
+        uint32_t w0[G::VWORDS], w1[G::VWORDS], w8[G::VWORDS], w9[G::VWORDS];  // tokens 2c, 2c+1, 2c+8, 2c+9
+        uint32_t sz0, sz1;  // half2 (scale, zero) of tokens r, r + 8
+    };
+    auto load_v = [&](const uint8_t* stage, VRegs& vr) {
+        ld_words(stage + v_off, vr.w0);
+        ld_words(stage + v_off + ROW, vr.w1);
+        ld_words(stage + v_off + 8 * ROW, vr.w8);
+        ld_words(stage + v_off + 9 * ROW, vr.w9);
+        vr.sz0 = static_cast<uint32_t>(ld16(stage + z_off)) | (static_cast<uint32_t>(ld16(stage + z_off + 2)) << 16);
+        vr.sz1 = static_cast<uint32_t>(ld16(stage + z_off + 8 * ROW)) |
+                 (static_cast<uint32_t>(ld16(stage + z_off + 8 * ROW + 2)) << 16);
+    };
 
     // ---- running state ---------------------------------------------------------------
     float o[G::MTILES][4];
@@ -359,171 +569,14 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     float z_acc[2] = {0.f, 0.f};
     const uint32_t bias_a = (r == 0) ? 0x3C003C00u : 0u;
     const uint32_t a_bias[4] = {bias_a, 0u, bias_a, 0u};
-    float* xch = reinterpret_cast<float*>(smem + G::X_OFF);  // [warp][lane][8]
 
-    const int nch = c1 - c0;
-    int bid[NS];
-#pragma unroll
-    for (int st = 0; st < NS; ++st) bid[st] = -1;
-#pragma unroll
-    for (int st = 0; st < NS - 1; ++st) {
-        if (st < nch) bid[st] = issue_next(st);
-        cp_async_commit();
-    }
-
-#pragma unroll 1
-    for (int base = 0; base < nch; base += NS) {
-#pragma unroll
-        for (int sl = 0; sl < NS; ++sl) {
-            const int it = base + sl;
-            if (it >= nch) break;
-            cp_async_wait<NS - 2>();
-            __syncthreads();
-            {
-                const int nslot = (sl + NS - 1) % NS;  // static once the loop is unrolled
-                if (it + NS - 1 < nch) bid[nslot] = issue_next(nslot);
-                cp_async_commit();
-            }
-            if (bid[sl] < 0) {
-                if (lane == 0 && warp == 0) set_flag(c.flags, kFlagBlock);
-                continue;
-            }
-            const int tok0 = (c0 + it) * kTok;
-            const uint8_t* stage = ring + sl * G::STAGE;
-            const bool v_r = tok0 + r < L;
-            const bool v_r8 = tok0 + r + 8 < L;
-
-            // ---- QK over this warp's share of the dims ------------------------------
-            // independent accumulators (even/odd k-step x hi/lo query part) keep
-            // the dependent-MMA chains short; summed after the loop
-            float qacc[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) qacc[i][e] = 0.f;
-            float nsq[2] = {0.f, 0.f};
-            float nacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
-                uint32_t kw0[G::KWORDS], kw1[G::KWORDS];
-                ld_words(stage + k_off, kw0);
-                ld_words(stage + k_off + 8 * ROW, kw1);
-#pragma unroll
-                for (int j = 0; j < G::KSTEPS; ++j) {
-                    uint32_t af[4];
-                    if constexpr (KB == 3) {
-                        // local pairs 2j (a0/a1) and 2j+1 (a2/a3): 6-bit fields at bit 6 * pair
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int bit = 6 * (2 * j + e);
-                            const int wi = bit / 32, off = bit % 32;
-                            uint32_t x0, x1;
-                            if (off + 6 <= 32) {
-                                x0 = off <= 8 ? (kw0[wi] << (8 - off)) : (kw0[wi] >> (off - 8));
-                                x1 = off <= 8 ? (kw1[wi] << (8 - off)) : (kw1[wi] >> (off - 8));
-                            } else {
-                                x0 = __funnelshift_r(kw0[wi], kw0[wi + 1], off - 8);
-                                x1 = __funnelshift_r(kw1[wi], kw1[wi + 1], off - 8);
-                            }
-                            const uint2 t0 = *reinterpret_cast<const uint2*>(lut + ((x0 & 0x3F00u) | lane8));
-                            const uint2 t1 = *reinterpret_cast<const uint2*>(lut + ((x1 & 0x3F00u) | lane8));
-                            af[2 * e] = t0.x;
-                            af[2 * e + 1] = t1.x;
-                            if constexpr (NC) {
-                                nsq[0] += __uint_as_float(t0.y);
-                                nsq[1] += __uint_as_float(t1.y);
-                            }
-                        }
-                    } else if constexpr (KB == 4) {
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int bit = 8 * (2 * j + e);
-                            const int wi = bit / 32, off = bit % 32;
-                            const uint32_t x0 = off <= 7 ? (kw0[wi] << (7 - off)) : (kw0[wi] >> (off - 7));
-                            const uint32_t x1 = off <= 7 ? (kw1[wi] << (7 - off)) : (kw1[wi] >> (off - 7));
-                            af[2 * e] = ld32(lut + ((x0 & 0x7F80u) | lane4));
-                            af[2 * e + 1] = ld32(lut + ((x1 & 0x7F80u) | lane4));
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int bit = 16 * (2 * j + e);
-                            const int wi = bit / 32, off = bit % 32;
-                            const __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
-                                static_cast<__nv_fp8x2_storage_t>((kw0[wi] >> off) & 0xffffu), __NV_E4M3);
-                            const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(
-                                static_cast<__nv_fp8x2_storage_t>((kw1[wi] >> off) & 0xffffu), __NV_E4M3);
-                            af[2 * e] = static_cast<uint32_t>(h0.x) | (static_cast<uint32_t>(h0.y) << 16);
-                            af[2 * e + 1] = static_cast<uint32_t>(h1.x) | (static_cast<uint32_t>(h1.y) << 16);
-                        }
-                    }
-                    // af = {tok r pair 2j, tok r+8 pair 2j, tok r pair 2j+1, tok r+8 pair 2j+1}
-                    const uint32_t afrag[4] = {af[0], af[1], af[2], af[3]};
-                    const uint4 qb = qfrag[j * qstride];
-                    mma16816(qacc[2 * (j & 1)], afrag, qb.x, qb.y);
-                    mma16816(qacc[2 * (j & 1) + 1], afrag, qb.z, qb.w);
-                    if constexpr (NC && KB == 4) {
-                        uint32_t sq[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __half2 x = *reinterpret_cast<const __half2*>(&afrag[e]);
-                            const __half2 y = __hmul2(x, x);
-                            sq[e] = *reinterpret_cast<const uint32_t*>(&y);
-                        }
-                        mma16816(nacc[j & 1], sq, 0x3C003C00u, 0x3C003C00u);  // every column: sum of squares
-                    }
-                }
-            }
-            float sacc[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[e] = (qacc[0][e] + qacc[2][e]) + (qacc[1][e] + qacc[3][e]);
-            float n0 = 0.f, n1 = 0.f;  // ||c~||^2 of tokens r, r + 8 (this warp's share)
-            if constexpr (NC && KB == 3) {
-                n0 = nsq[0] + __shfl_xor_sync(kFull, nsq[0], 1);
-                n0 += __shfl_xor_sync(kFull, n0, 2);
-                n1 = nsq[1] + __shfl_xor_sync(kFull, nsq[1], 1);
-                n1 += __shfl_xor_sync(kFull, n1, 2);
-            } else if constexpr (NC && KB == 4) {
-                n0 = nacc[0][0] + nacc[1][0];
-                n1 = nacc[0][2] + nacc[1][2];
-            }
-            if constexpr (WPH > 1) {
-                // add the other warps' shares of the dims
-                float4* mine = reinterpret_cast<float4*>(xch + (warp * 32 + lane) * 8);
-                mine[0] = make_float4(sacc[0], sacc[1], sacc[2], sacc[3]);
-                mine[1] = make_float4(n0, n1, 0.f, 0.f);
-                group_barrier(1 + h, 32 * WPH);
-#pragma unroll
-                for (int w = 1; w < WPH; ++w) {
-                    const int ow = h * WPH + (part + w) % WPH;
-                    const float4* other = reinterpret_cast<const float4*>(xch + (ow * 32 + lane) * 8);
-                    const float4 os = other[0];
-                    const float4 on = other[1];
-                    sacc[0] += os.x;
-                    sacc[1] += os.y;
-                    sacc[2] += os.z;
-                    sacc[3] += os.w;
-                    n0 += on.x;
-                    n1 += on.y;
-                }
-            }
-
-            // ---- per-token factors: vec_norm, norm correction, masking -------------
-            float f_r = 1.f, f_r8 = 1.f;
-            if constexpr (KB != 8) {
-                f_r = half_from_bits(ld16(stage + n_off));
-                f_r8 = half_from_bits(ld16(stage + n_off + 8 * ROW));
-                if constexpr (NC) {
-                    f_r *= rsqrtf(n0);
-                    f_r8 *= rsqrtf(n1);
-                }
-            }
-            float sc[4];
-            sc[0] = v_r ? sacc[0] * f_r : -INFINITY;
-            sc[1] = v_r ? sacc[1] * f_r : -INFINITY;
-            sc[2] = v_r8 ? sacc[2] * f_r8 : -INFINITY;
-            sc[3] = v_r8 ? sacc[3] * f_r8 : -INFINITY;
-
-            // ---- online softmax (log2 domain), lazy rescale ---------------------------
+    // ---- online softmax and P.V of one chunk (scores sc, values vr) -------------
+    auto rescale = [&](const float (&sc)[4]) {
+        // lazy rescale: the reference max moves only when a score passes it by
+        // more than 2^8; a per-lane test, reduced across the warp only then
+        const bool grow = (sc[0] > m_ref[0] + kRescaleThreshold) || (sc[2] > m_ref[0] + kRescaleThreshold) ||
+                          (sc[1] > m_ref[1] + kRescaleThreshold) || (sc[3] > m_ref[1] + kRescaleThreshold);
+        if (__any_sync(kFull, grow)) {
             float mx0 = fmaxf(sc[0], sc[2]);
             float mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
@@ -531,86 +584,146 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
                 mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, m));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, m));
             }
-            const bool grow = (mx0 > m_ref[0] + kRescaleThreshold) || (mx1 > m_ref[1] + kRescaleThreshold);
-            if (__any_sync(kFull, grow)) {
-                const float n0m = fmaxf(m_ref[0], mx0);
-                const float n1m = fmaxf(m_ref[1], mx1);
-                const float al0 = (n0m == -INFINITY) ? 1.f : fast_exp2(m_ref[0] - n0m);
-                const float al1 = (n1m == -INFINITY) ? 1.f : fast_exp2(m_ref[1] - n1m);
+            const float n0m = fmaxf(m_ref[0], mx0);
+            const float n1m = fmaxf(m_ref[1], mx1);
+            const float al0 = (n0m == -INFINITY) ? 1.f : fast_exp2(m_ref[0] - n0m);
+            const float al1 = (n1m == -INFINITY) ? 1.f : fast_exp2(m_ref[1] - n1m);
 #pragma unroll
-                for (int mt = 0; mt < G::MTILES; ++mt) {
-                    o[mt][0] *= al0;
-                    o[mt][1] *= al1;
-                    o[mt][2] *= al0;
-                    o[mt][3] *= al1;
-                }
-                ob[0] *= al0;
-                ob[1] *= al1;
-                ob[2] *= al0;
-                ob[3] *= al1;
-                l_acc[0] *= al0;
-                l_acc[1] *= al1;
-                z_acc[0] *= al0;
-                z_acc[1] *= al1;
-                m_ref[0] = n0m;
-                m_ref[1] = n1m;
+            for (int mt = 0; mt < G::MTILES; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
             }
-            float pr[4];
-            pr[0] = (sc[0] == -INFINITY) ? 0.f : fast_exp2(sc[0] - m_ref[0]);
-            pr[1] = (sc[1] == -INFINITY) ? 0.f : fast_exp2(sc[1] - m_ref[1]);
-            pr[2] = (sc[2] == -INFINITY) ? 0.f : fast_exp2(sc[2] - m_ref[0]);
-            pr[3] = (sc[3] == -INFINITY) ? 0.f : fast_exp2(sc[3] - m_ref[1]);
-            l_acc[0] += pr[0] + pr[2];
-            l_acc[1] += pr[1] + pr[3];
+            ob[0] *= al0;
+            ob[1] *= al1;
+            ob[2] *= al0;
+            ob[3] *= al1;
+            l_acc[0] *= al0;
+            l_acc[1] *= al1;
+            z_acc[0] *= al0;
+            z_acc[1] *= al1;
+            m_ref[0] = n0m;
+            m_ref[1] = n1m;
+        }
+    };
+    auto softmax_pv = [&](const float (&sc)[4], const VRegs& vr, int tok0, bool ok) {
+        // After the rescale test every column's reference max is finite or all its
+        // scores are -inf; exp2(-inf) = 0 masks past-the-end tokens.
+        float pr[4];
+        pr[0] = fast_exp2(sc[0] - m_ref[0]);
+        pr[1] = fast_exp2(sc[1] - m_ref[1]);
+        pr[2] = fast_exp2(sc[2] - m_ref[0]);
+        pr[3] = fast_exp2(sc[3] - m_ref[1]);
+        if (m_ref[0] == -INFINITY) pr[0] = pr[2] = 0.f;
+        if (m_ref[1] == -INFINITY) pr[1] = pr[3] = 0.f;
+        l_acc[0] += pr[0] + pr[2];
+        l_acc[1] += pr[1] + pr[3];
 
-            // value scale / zero of tokens r and r + 8
-            float vs_r = 0.f, vz_r = 0.f, vs_r8 = 0.f, vz_r8 = 0.f;
-            {
-                const uint32_t sz0 = static_cast<uint32_t>(ld16(stage + z_off)) |
-                                     (static_cast<uint32_t>(ld16(stage + z_off + 2)) << 16);
-                const uint32_t sz1 = static_cast<uint32_t>(ld16(stage + z_off + 8 * ROW)) |
-                                     (static_cast<uint32_t>(ld16(stage + z_off + 8 * ROW + 2)) << 16);
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&sz0));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&sz1));
-                if (v_r) {
-                    vs_r = f0.x;
-                    vz_r = f0.y;
-                }
-                if (v_r8) {
-                    vs_r8 = f1.x;
-                    vz_r8 = f1.y;
-                }
-            }
-            // zero point plus the centre of the code range (codes enter centred)
-            const float zc_r = vz_r + kCentre * vs_r;
-            const float zc_r8 = vz_r8 + kCentre * vs_r8;
-            z_acc[0] += pr[0] * zc_r + pr[2] * zc_r8;
-            z_acc[1] += pr[1] * zc_r + pr[3] * zc_r8;
-            const uint32_t pb0 = movmatrix_trans(pack_half2(pr[0] * vs_r, pr[1] * vs_r));
-            const uint32_t pb1 = movmatrix_trans(pack_half2(pr[2] * vs_r8, pr[3] * vs_r8));
+        // value scale / zero of tokens r and r + 8 (0 past the end)
+        const bool v_r = ok && tok0 + r < L;
+        const bool v_r8 = ok && tok0 + r + 8 < L;
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&vr.sz0));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&vr.sz1));
+        const float vs_r = v_r ? f0.x : 0.f, vz_r = v_r ? f0.y : 0.f;
+        const float vs_r8 = v_r8 ? f1.x : 0.f, vz_r8 = v_r8 ? f1.y : 0.f;
+        // zero point plus the centre of the code range (codes enter centred)
+        const float zc_r = fmaf(kCentre, vs_r, vz_r);
+        const float zc_r8 = fmaf(kCentre, vs_r8, vz_r8);
+        z_acc[0] = fmaf(pr[0], zc_r, fmaf(pr[2], zc_r8, z_acc[0]));
+        z_acc[1] = fmaf(pr[1], zc_r, fmaf(pr[3], zc_r8, z_acc[1]));
+        const uint32_t pb0 = movmatrix_trans(pack_half2(pr[0] * vs_r, pr[1] * vs_r));
+        const uint32_t pb1 = movmatrix_trans(pack_half2(pr[2] * vs_r8, pr[3] * vs_r8));
 
-            // ---- P.V over this warp's share of the dims --------------------------------
-            {
-                uint32_t w0[G::VWORDS], w1[G::VWORDS], w8[G::VWORDS], w9[G::VWORDS];
-                ld_words(stage + v_off, w0);
-                ld_words(stage + v_off + ROW, w1);
-                ld_words(stage + v_off + 8 * ROW, w8);
-                ld_words(stage + v_off + 9 * ROW, w9);
+        // P.V over this warp's share of the dims: codes enter as fp16
+        // subnormals code * 2^(pos - 24), masked in place
 #pragma unroll
-                for (int mt = 0; mt < G::MTILES; ++mt) {
-                    uint32_t vf[4];
-                    vf[0] = value_pair<VB>(w0, w1, 2 * mt);
-                    vf[1] = value_pair<VB>(w0, w1, 2 * mt + 1);
-                    vf[2] = value_pair<VB>(w8, w9, 2 * mt);
-                    vf[3] = value_pair<VB>(w8, w9, 2 * mt + 1);
-                    mma16816(o[mt], vf, pb0, pb1);
+        for (int mt = 0; mt < G::MTILES; ++mt) {
+            uint32_t vf[4];
+            vf[0] = value_sub<VB>(vr.w0, vr.w1, 2 * mt);
+            vf[1] = value_sub<VB>(vr.w0, vr.w1, 2 * mt + 1);
+            vf[2] = value_sub<VB>(vr.w8, vr.w9, 2 * mt);
+            vf[3] = value_sub<VB>(vr.w8, vr.w9, 2 * mt + 1);
+            mma16816(o[mt], vf, pb0, pb1);
+        }
+        mma16816(ob, a_bias, pb0, pb1);
+    };
+
+    // ---- main loop: QK of chunk it and the softmax and P.V of chunk it - 1 form
+    // one straight-line block; waits and the rare rescale sit outside it -------
+    // After a wait gives up, the warp stops waiting and runs on with every
+    // chunk masked, so that warps sharing a head still meet at each exchange.
+    bool timed_out = false;
+    auto acquire = [&](int it, int& blk) -> const uint8_t* {
+        const int slot = it % NS;
+        blk = -1;
+        if (!timed_out) {
+            if (mbar_wait(full_bar(slot), static_cast<uint32_t>((it / NS) & 1))) blk = stage_blk[slot];
+            else timed_out = true;
+        }
+        return ring + slot * G::STAGE;
+    };
+    auto release = [&](int it) {
+        __syncwarp();
+        if (lane == 0) {
+            const int slot = it % NS;
+            if (atom_add_acq_rel(cnt_addr(slot), 1u) == static_cast<uint32_t>(G::NWARPS - 1)) {
+                *reinterpret_cast<volatile uint32_t*>(ctrl + 8 * NS + 4 * slot) = 0u;
+                if (it + NS < nch) {
+                    fence_proxy_async();
+                    issue(it + NS);
                 }
-                mma16816(ob, a_bias, pb0, pb1);
             }
         }
+    };
+    float sc_prev[4];
+    VRegs v_prev;
+    bool ok_prev = false;
+    if (nch > 0) {
+        int blk = -1;
+        const uint8_t* stage = acquire(0, blk);
+        ok_prev = blk >= 0;
+        qk(stage, c0 * kTok, ok_prev, 0, sc_prev);
+        load_v(stage, v_prev);
+        release(0);
     }
-    cp_async_wait<0>();
-
+#pragma unroll 1
+    for (int it = 1; it < nch; ++it) {
+        int blk = -1;
+        const uint8_t* stage = acquire(it, blk);
+        if (!ok_prev && !timed_out && lane == 0 && warp == 0) set_flag(c.flags, kFlagBlock);
+        rescale(sc_prev);
+        const bool ok = blk >= 0;
+        float sc_cur[4];
+        VRegs v_cur;
+        qk(stage, (c0 + it) * kTok, ok, it & 1, sc_cur);
+        load_v(stage, v_cur);
+        softmax_pv(sc_prev, v_prev, (c0 + it - 1) * kTok, ok_prev);
+        release(it);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc_prev[e] = sc_cur[e];
+        v_prev = v_cur;
+        ok_prev = ok;
+    }
+    if (nch > 0) {
+        if (!ok_prev && !timed_out && lane == 0 && warp == 0) set_flag(c.flags, kFlagBlock);
+        rescale(sc_prev);
+        softmax_pv(sc_prev, v_prev, (c1 - 1) * kTok, ok_prev);
+    }
+    if (timed_out) {
+        if (lane == 0) {
+            set_flag(c.flags, kFlagWait);
+            atomicExch(err_word, 1);
+        }
+    }
+    // A CTA must not exit with bulk copies into its shared memory in flight.
+    // Normally every issued chunk has been consumed; after a timed-out wait,
+    // thread 0 waits (bounded) for the stages' last phases.
+    __syncthreads();
+    if (threadIdx.x == 0 && *reinterpret_cast<volatile int*>(err_word) != 0) {
+        for (int it = nch - 1; it >= 0 && it >= nch - NS; --it)
+            mbar_wait(full_bar(it % NS), static_cast<uint32_t>((it / NS) & 1));
+    }
     // ---- partial state ------------------------------------------------------------------
 #pragma unroll
     for (int m = 4; m < 32; m <<= 1) {
@@ -631,14 +744,14 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
             part_out[0] = m_ref[e];
             part_out[1] = l_acc[e];
         }
-        const float bias = e ? bias1 : bias0;
+        const float cb = kCentre * (e ? bias1 : bias0);
         const float z = z_acc[e];
 #pragma unroll
         for (int mt = 0; mt < G::MTILES; ++mt) {
-            // sum P'(code - centre) = 2^VB (o - bias) - centre * bias
+            // sum P'(code - centre) = o * 2^(24 - pos) - centre * bias
             const int d0 = r * (D / 8) + 2 * (part * G::MTILES + mt);
-            part_out[2 + d0] = (o[mt][e] - bias) * kValW - kCentre * bias + z;
-            part_out[2 + d0 + 1] = (o[mt][2 + e] - bias) * kValW - kCentre * bias + z;
+            part_out[2 + d0] = fmaf(o[mt][e], value_weight<VB>(2 * mt), -cb) + z;
+            part_out[2 + d0 + 1] = fmaf(o[mt][2 + e], value_weight<VB>(2 * mt + 1), -cb) + z;
         }
     }
 }
@@ -666,7 +779,7 @@ struct Policy {
     static constexpr int WPH = pick_wph<D, KB, VB>(kWphRaw < 1 ? 1 : (kWphRaw > kWphMax ? kWphMax : kWphRaw));
     static constexpr int MINB = 32 * H * WPH > 256 ? 1 : 2;
     static constexpr int kBudget = MINB == 1 ? 220 * 1024 : 110 * 1024;
-    using G1 = Geo<D, KB, VB, H, WPH, 1>;
+    using G1 = Geo<D, KB, VB, H, WPH, 8>;
     // fixed part plus the query fragments of up to 5 query heads per KV head
     static constexpr int kFixed = G1::RING_OFF + 16 + H * 5 * D * 4;
     static constexpr int kNs = (kBudget - kFixed) / G1::STAGE;

@@ -39,6 +39,7 @@ struct CacheGeom {
 constexpr uint32_t kFlagSlot = 1u;
 constexpr uint32_t kFlagBlock = 2u;
 constexpr uint32_t kFlagSeq = 4u;
+constexpr uint32_t kFlagWait = 8u;
 
 struct DecodePlan {
     int32_t num_splits;
