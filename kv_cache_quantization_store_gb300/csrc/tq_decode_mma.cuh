@@ -67,6 +67,7 @@ struct Args {
     int num_splits;
     float qscale;     // sm_scale * log2(e)
     float lut_scale;  // table value = centroid * lut_scale (= gamma * sqrt(d))
+    int tok_eo;       // token order of the chunk rows: 0 natural, 1 even tokens then odd tokens
 };
 
 // One-dimensional bulk copy global -> shared that signals completion on an
@@ -152,18 +153,35 @@ __device__ __forceinline__ void group_barrier(int id, int nthreads) {
 __device__ __forceinline__ uint32_t ld32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ uint16_t ld16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 
-// NW consecutive little-endian words starting at any byte address of shared
-// memory (reads one aligned word past the range; the ring carries padding).
+// NW consecutive little-endian words starting at byte `off` of a 4-byte
+// aligned shared buffer (reads one aligned word past the range; the ring
+// carries padding).  Plain pointer arithmetic on the shared buffer keeps the
+// loads in the shared state space.
 template <int NW>
-__device__ __forceinline__ void ld_words(const uint8_t* p, uint32_t (&w)[NW]) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint8_t* base = p - (a & 3u);
-    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
+__device__ __forceinline__ void ld_words(const uint8_t* base, int off, uint32_t (&w)[NW]) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(base + (off & ~3));
+    const uint32_t sh = static_cast<uint32_t>(off & 3) * 8u;
     uint32_t raw[NW + 1];
 #pragma unroll
-    for (int i = 0; i <= NW; ++i) raw[i] = ld32(base + 4 * i);
+    for (int i = 0; i <= NW; ++i) raw[i] = p[i];
 #pragma unroll
     for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
+}
+
+// One code unit of U bytes (2 or 4) from shared memory, zero-extended.
+template <int U>
+__device__ __forceinline__ uint32_t ld_unit(const uint8_t* p) {
+    if constexpr (U == 4) return *reinterpret_cast<const uint32_t*>(p);
+    else return *reinterpret_cast<const uint16_t*>(p);
+}
+
+// 4-bit value codes of two tokens' units (token a in the low half, token b in
+// the high half) as fp16 subnormals: the code of dim w of the unit stays in
+// place inside byte w / 2, i.e. code * 2^(4 (w % 2) - 24).
+__device__ __forceinline__ uint32_t value_unit_sub(uint32_t ua, uint32_t ub, int w) {
+    const int b = w / 2, pos = 4 * (w % 2);
+    const uint32_t win = prmt(ua, ub, b | (b << 4) | ((b + 4) << 8) | ((b + 4) << 12));
+    return win & ((0xFu << pos) * 0x00010001u);
 }
 
 // Value code of local dim n for two tokens as an fp16 subnormal pair
@@ -200,7 +218,7 @@ __device__ __forceinline__ constexpr float value_weight(int n) {
 
 // Compile-time geometry of one kernel instantiation.  Shared memory:
 // [pair table][score exchange x2][control][16 zero bytes][stage ring][Q' fragments].
-template <int D, int KB, int VB, int H, int WPH, int NS>
+template <int D, int KB, int VB, int H, int WPH, int NS, bool PACKQ>
 struct Geo {
     using S = Slot<D, KB, VB>;
     static constexpr int SA = S::kAligned;
@@ -216,9 +234,22 @@ struct Geo {
     static constexpr int KWORDS = (KBYTES_W + 3) / 4;
     static constexpr int VBITS_W = (D / 8 / WPH) * VB;  // value code bits of one thread, token and warp
     static constexpr int VWORDS = (VBITS_W + 31) / 32;
-    static constexpr int LUT_ENTRY = KB == 3 ? 8 : 4;
+    // Lane layout of the code loads.  Unit layouts: lane c (keys) or r
+    // (values) reads units c + 4m or r + 8m of its warp's contiguous share of
+    // the slot, so that neighbouring lanes hit neighbouring banks; a unit is 4
+    // bytes where every share starts 4-byte aligned, else 2.  3-bit codes keep
+    // one contiguous block per lane.
+    static constexpr bool KUNITS = KB != 3;
+    static constexpr int KUNIT = KB == 8 ? 4 : 2;   // bytes: the 4 dims of one k-step
+    static constexpr int KSH = (D / WPH) * KB / 8;  // key code bytes of a warp's share
+    static constexpr bool VUNITS = VB == 4;
+    static constexpr int VSH = (D / WPH) * VB / 8;  // value code bytes of a warp's share
+    static constexpr int VUNIT = (SA % 4 == 0 && S::kKeyBytes % 4 == 0 && VSH % 32 == 0) ? 4 : 2;
+    static constexpr int VDPU = 2 * VUNIT;          // 4-bit value dims per unit
+    static constexpr int VNU = VSH / (8 * VUNIT);   // value units of one lane and token
+    static constexpr int VREGS = VUNITS ? VNU : VWORDS;
     static constexpr int LUT_ENTRIES = KB == 3 ? 64 : (KB == 4 ? 256 : 0);
-    static constexpr int LUT_BYTES = LUT_ENTRIES * 32 * LUT_ENTRY;
+    static constexpr int LUT_BYTES = LUT_ENTRIES * 32 * 4;  // half2 per entry and lane
     static constexpr int XCH_W = WPH > 1 ? 32 * 8 * 4 : 0;  // per warp and buffer
     static constexpr int X_OFF = LUT_BYTES;
     // control block: full mbarrier, release counter, block id per stage; error word
@@ -227,19 +258,22 @@ struct Geo {
     static constexpr int ZERO_OFF = CTRL_OFF + CTRL_BYTES;
     static constexpr int RING_OFF = ZERO_OFF + 16;
     static constexpr int RING = NS * STAGE + 16;
-    // Q' fragments follow the ring: per warp, k-step and query row r < G,
-    // 4 lanes x {hi0, hi1, lo0, lo1}, i.e. G * d * 4 bytes per KV head.
+    // Q' fragments follow the ring.  PACKQ (G <= 4): per warp and k-step one
+    // {b0, b1} per lane, columns 0-3 the hi parts and 4-7 the lo parts of the
+    // queries (d * 16 bytes per KV head).  Otherwise per warp, k-step and
+    // query row r < G, 4 lanes x {hi0, hi1, lo0, lo1} (G * d * 4 bytes per KV head).
     __host__ __device__ static int q_off(int hq) {
         const int qrot = hq * D * 4;  // the ring also holds the fp32 query rotation
         return RING_OFF + (RING > qrot ? RING : qrot);
     }
-    __host__ __device__ static int smem_bytes(int hq) { return q_off(hq) + hq * D * 4; }
+    __host__ __device__ static int q_bytes(int hq) { return PACKQ ? H * D * 16 : hq * D * 4; }
+    __host__ __device__ static int smem_bytes(int hq) { return q_off(hq) + q_bytes(hq); }
 };
 
-template <int D, int KB, int VB, bool NC, int H, int WPH, int NS, int MINB>
+template <int D, int KB, int VB, bool NC, int H, int WPH, int NS, int MINB, bool PACKQ>
 __global__ void __launch_bounds__(32 * H * WPH, MINB)
 decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
-    using G = Geo<D, KB, VB, H, WPH, NS>;
+    using G = Geo<D, KB, VB, H, WPH, NS, PACKQ>;
     using S = typename G::S;
     static_assert(((D / 4 / WPH) * KB) % 8 == 0 && ((D / 8 / WPH) * VB) % 8 == 0,
                   "a warp's share of the codes must start on a byte");
@@ -287,24 +321,23 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 
     // ---- pair lookup table: centroids * lut_scale as fp16, one copy per lane ----
     const float ls = a.lut_scale;
-    if constexpr (KB == 3) {
-        // 64 entries x 32 lanes x 8 bytes; one 16-byte store writes two lanes' copies
-        for (int i = threadIdx.x; i < 64 * 16; i += NT) {
-            const int e = i >> 4;
-            const uint32_t hv = pack_half2(p.centroids[e & 7] * ls, p.centroids[e >> 3] * ls);
-            const float ra = __low2float(*reinterpret_cast<const __half2*>(&hv));
-            const float rb = __high2float(*reinterpret_cast<const __half2*>(&hv));
-            const uint32_t n2 = __float_as_uint(ra * ra + rb * rb);  // as the MMA sees the pair
-            reinterpret_cast<uint4*>(smem)[i] = make_uint4(hv, n2, hv, n2);
-        }
-    } else if constexpr (KB == 4) {
-        // 256 entries x 32 lanes x 4 bytes; one 16-byte store writes four lanes' copies
-        for (int i = threadIdx.x; i < 256 * 8; i += NT) {
+    if constexpr (KB == 3 || KB == 4) {
+        // entry e = codes (e & mask, e >> bits) of a dim pair, 32 lanes x 4 bytes;
+        // one 16-byte store writes four lanes' copies
+        constexpr int kBits = KB, kMask = (1 << KB) - 1;
+        for (int i = threadIdx.x; i < G::LUT_ENTRIES * 8; i += NT) {
             const int e = i >> 3;
-            const uint32_t hv = pack_half2(p.centroids[e & 15] * ls, p.centroids[e >> 4] * ls);
+            const uint32_t hv = pack_half2(p.centroids[e & kMask] * ls, p.centroids[e >> kBits] * ls);
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(hv, hv, hv, hv);
         }
     }
+
+    // First of the 4 consecutive key dims lane c of warp part covers at local
+    // k-step jl (the lane layout of the key loads).
+    auto key_dim0 = [](int c_, int part_, int jl) -> int {
+        if constexpr (G::KUNITS) return part_ * (D / WPH) + 4 * (c_ + 4 * jl);
+        else return c_ * (D / 4) + part_ * (D / (4 * WPH)) + 4 * jl;
+    };
 
     // ---- queries: q' = Pi q (MSE keys), scaled, into B fragments ---------------
     {
@@ -339,23 +372,45 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         // is divided out here (with NC it cancels in c / ||c||).
         float f = a.qscale;
         if constexpr (KB != 8) f *= rsqrtf(static_cast<float>(D)) * (NC ? 1.0f : 1.0f / ls);
-        const float* qrow = qs + (h * Gq + r) * D;
-        // fragments of this warp: [k-step][query row r < G][lane c]
-        uint4* dst = reinterpret_cast<uint4*>(smem + G::q_off(Hq)) + warp * G::KSTEPS * Gq * 4;
-        if (threadIdx.x == 0) *reinterpret_cast<uint4*>(smem + G::ZERO_OFF) = make_uint4(0u, 0u, 0u, 0u);
-        for (int jl = 0; jl < G::KSTEPS && r < Gq; ++jl) {
-            const int j = part * G::KSTEPS + jl;  // k-step of the whole head
-            const int u = cc * (D / 8) + 2 * j;   // pair index of b0; b1 is u + 1
-            const float x0 = qrow[2 * u] * f, x1 = qrow[2 * u + 1] * f;
-            const float x2 = qrow[2 * u + 2] * f, x3 = qrow[2 * u + 3] * f;
-            const uint32_t hi0 = pack_half2(x0, x1);
-            const uint32_t hi1 = pack_half2(x2, x3);
-            const __half2 h0 = *reinterpret_cast<const __half2*>(&hi0);
-            const __half2 h1 = *reinterpret_cast<const __half2*>(&hi1);
-            const uint32_t lo0 = pack_half2(x0 - __low2float(h0), x1 - __high2float(h0));
-            const uint32_t lo1 = pack_half2(x2 - __low2float(h1), x3 - __high2float(h1));
-            dst[(jl * Gq + r) * 4 + cc] = make_uint4(hi0, hi1, lo0, lo1);
+        if constexpr (PACKQ) {
+            // column r of the B operand: query r & 3 of this head, hi part for
+            // r < 4 and lo part for r >= 4; zero past the G queries
+            const int qi = r & 3;
+            const bool real = qi < Gq;
+            const float* qrow = qs + (h * Gq + (real ? qi : 0)) * D;
+            uint2* dst = reinterpret_cast<uint2*>(smem + G::q_off(Hq)) + warp * G::KSTEPS * 32;
+            for (int jl = 0; jl < G::KSTEPS; ++jl) {
+                const int dm = key_dim0(cc, part, jl);  // b0: dims dm, dm + 1; b1: dm + 2, dm + 3
+                const float x0 = qrow[dm] * f, x1 = qrow[dm + 1] * f;
+                const float x2 = qrow[dm + 2] * f, x3 = qrow[dm + 3] * f;
+                const uint32_t hi0 = pack_half2(x0, x1);
+                const uint32_t hi1 = pack_half2(x2, x3);
+                const __half2 h0 = *reinterpret_cast<const __half2*>(&hi0);
+                const __half2 h1 = *reinterpret_cast<const __half2*>(&hi1);
+                const uint32_t lo0 = pack_half2(x0 - __low2float(h0), x1 - __high2float(h0));
+                const uint32_t lo1 = pack_half2(x2 - __low2float(h1), x3 - __high2float(h1));
+                uint2 v = r < 4 ? make_uint2(hi0, hi1) : make_uint2(lo0, lo1);
+                if (!real) v = make_uint2(0u, 0u);
+                dst[jl * 32 + lane] = v;
+            }
+        } else {
+            const float* qrow = qs + (h * Gq + r) * D;
+            // fragments of this warp: [k-step][query row r < G][lane c]
+            uint4* dst = reinterpret_cast<uint4*>(smem + G::q_off(Hq)) + warp * G::KSTEPS * Gq * 4;
+            for (int jl = 0; jl < G::KSTEPS && r < Gq; ++jl) {
+                const int dm = key_dim0(cc, part, jl);  // b0: dims dm, dm + 1; b1: dm + 2, dm + 3
+                const float x0 = qrow[dm] * f, x1 = qrow[dm + 1] * f;
+                const float x2 = qrow[dm + 2] * f, x3 = qrow[dm + 3] * f;
+                const uint32_t hi0 = pack_half2(x0, x1);
+                const uint32_t hi1 = pack_half2(x2, x3);
+                const __half2 h0 = *reinterpret_cast<const __half2*>(&hi0);
+                const __half2 h1 = *reinterpret_cast<const __half2*>(&hi1);
+                const uint32_t lo0 = pack_half2(x0 - __low2float(h0), x1 - __high2float(h0));
+                const uint32_t lo1 = pack_half2(x2 - __low2float(h1), x3 - __high2float(h1));
+                dst[(jl * Gq + r) * 4 + cc] = make_uint4(hi0, hi1, lo0, lo1);
+            }
         }
+        if (threadIdx.x == 0) *reinterpret_cast<uint4*>(smem + G::ZERO_OFF) = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
     }
     // lanes of padded query rows (r >= G) read the zero block at every k-step
@@ -364,6 +419,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
                                       r * 4 + cc
                                 : reinterpret_cast<const uint4*>(smem + G::ZERO_OFF);
     const int qstride = q_real ? Gq * 4 : 0;
+    const uint2* qfrag2 = reinterpret_cast<const uint2*>(smem + G::q_off(Hq)) + warp * G::KSTEPS * 32 + lane;
 
     // ---- chunk staging.  Chunk it (of this split) lives in stage it % NS; one
     // thread copies all of it (16 token rows of every head, contiguous in the
@@ -400,85 +456,98 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         for (int it = 0; it < NS && it < nch; ++it) issue(it);
     }
 
-    // ---- per-thread constant offsets inside a stage ---------------------------------
+    // ---- per-thread constant offsets inside a stage.  Row k of the MMA tiles
+    // holds token sig(k) of the chunk; the order is chosen on the host to
+    // spread each warp's loads over the shared-memory banks. -------------------
+    auto sig = [&](int k) -> int { return a.tok_eo ? (k < 8 ? 2 * k : 2 * (k - 8) + 1) : k; };
+    const int tq0 = sig(r), tq1 = sig(r + 8);  // QK rows r, r + 8
     const int hs = h * SA;
-    const int k_off = r * ROW + hs + cc * G::KBYTES + part * G::KBYTES_W;  // token r; +8 ROW for r+8
-    const int n_off = r * ROW + hs + S::kKeyIdxBytes;                     // vec_norm of token r
-    const int z_off = r * ROW + hs + S::kKeyBytes + S::kValCodeBytes;     // scale, zero of token r
-    const int v_off = 2 * cc * ROW + hs + S::kKeyBytes + (r * (D / 8) * VB + part * G::VBITS_W) / 8;
+    const int kbase = G::KUNITS ? hs + part * G::KSH + G::KUNIT * cc : hs + cc * G::KBYTES + part * G::KBYTES_W;
+    const int k_off0 = tq0 * ROW + kbase, k_off1 = tq1 * ROW + kbase;
+    const int n_off0 = tq0 * ROW + hs + S::kKeyIdxBytes, n_off1 = tq1 * ROW + hs + S::kKeyIdxBytes;
+    const int z_off0 = tq0 * ROW + hs + S::kKeyBytes + S::kValCodeBytes;
+    const int z_off1 = tq1 * ROW + hs + S::kKeyBytes + S::kValCodeBytes;
+    const int vbase = G::VUNITS ? hs + S::kKeyBytes + part * G::VSH + G::VUNIT * r
+                                : hs + S::kKeyBytes + (r * (D / 8) * VB + part * G::VBITS_W) / 8;
+    // P.V k-columns 2c, 2c + 1, 2c + 8, 2c + 9
+    const int v_off0 = sig(2 * cc) * ROW + vbase, v_off1 = sig(2 * cc + 1) * ROW + vbase;
+    const int v_off8 = sig(2 * cc + 8) * ROW + vbase, v_off9 = sig(2 * cc + 9) * ROW + vbase;
     const uint8_t* lut = smem;
     const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
-    const uint32_t lane8 = static_cast<uint32_t>(lane) << 3;
     float* xch = reinterpret_cast<float*>(smem + G::X_OFF);  // [buffer][warp][lane][8]
 
     // ---- QK of one staged chunk: log2-domain scores of tokens r, r + 8 for
     // query columns 2c, 2c + 1, -inf past the sequence end ---------------------------
     auto qk = [&](const uint8_t* stage, int tok0, bool ok, int buf, float (&sc)[4]) {
-        float qacc[2][4];  // hi and lo query parts
+        float qacc[2][4];  // hi and lo query parts (PACKQ: even and odd k-steps)
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int e = 0; e < 4; ++e) qacc[i][e] = 0.f;
-        float nsq[2] = {0.f, 0.f};
         float nacc[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t kw0[G::KWORDS], kw1[G::KWORDS];
-        ld_words(stage + k_off, kw0);
-        ld_words(stage + k_off + 8 * ROW, kw1);
+        constexpr int KREGS = G::KUNITS ? G::KSTEPS : G::KWORDS;
+        uint32_t kw0[KREGS], kw1[KREGS];
+        if constexpr (G::KUNITS) {
+#pragma unroll
+            for (int m = 0; m < KREGS; ++m) {
+                kw0[m] = ld_unit<G::KUNIT>(stage + k_off0 + 4 * G::KUNIT * m);
+                kw1[m] = ld_unit<G::KUNIT>(stage + k_off1 + 4 * G::KUNIT * m);
+            }
+        } else {
+            ld_words(stage, k_off0, kw0);
+            ld_words(stage, k_off1, kw1);
+        }
 #pragma unroll
         for (int j = 0; j < G::KSTEPS; ++j) {
-            // a = {tok r pair 2j, tok r+8 pair 2j, tok r pair 2j+1, tok r+8 pair 2j+1}
+            // a = {row r dims 0-1, row r+8 dims 0-1, row r dims 2-3, row r+8 dims 2-3}
+            // of the 4 dims this lane covers at k-step j
             uint32_t af[4];
-            if constexpr (KB == 3) {
-                // 6-bit pair codes at bit 6 * pair; table entry {half2 c, float c0^2 + c1^2}
+            if constexpr (KB == 8) {
+                // unit j: 4 FP8 codes
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
+                        static_cast<__nv_fp8x2_storage_t>((kw0[j] >> (16 * e)) & 0xffffu), __NV_E4M3);
+                    const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(
+                        static_cast<__nv_fp8x2_storage_t>((kw1[j] >> (16 * e)) & 0xffffu), __NV_E4M3);
+                    af[2 * e] = static_cast<uint32_t>(h0.x) | (static_cast<uint32_t>(h0.y) << 16);
+                    af[2 * e + 1] = static_cast<uint32_t>(h1.x) | (static_cast<uint32_t>(h1.y) << 16);
+                }
+            } else if constexpr (KB == 4) {
+                // unit j: two pair codes, one per byte, moved to bit 7 (table rows of 128 bytes)
+                af[0] = ld32(lut + (((kw0[j] << 7) & 0x7F80u) | lane4));
+                af[1] = ld32(lut + (((kw1[j] << 7) & 0x7F80u) | lane4));
+                af[2] = ld32(lut + (((kw0[j] >> 1) & 0x7F80u) | lane4));
+                af[3] = ld32(lut + (((kw1[j] >> 1) & 0x7F80u) | lane4));
+            } else {
+                // 6-bit pair codes at bit 6 * pair of the lane's block, moved to bit 7
+                constexpr uint32_t kIdx = 0x3Fu << 7;
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int bit = 6 * (2 * j + e);
                     const int wi = bit / 32, off = bit % 32;
                     uint32_t x0, x1;
                     if (off + 6 <= 32) {
-                        x0 = off <= 8 ? (kw0[wi] << (8 - off)) : (kw0[wi] >> (off - 8));
-                        x1 = off <= 8 ? (kw1[wi] << (8 - off)) : (kw1[wi] >> (off - 8));
+                        x0 = off <= 7 ? (kw0[wi] << (7 - off)) : (kw0[wi] >> (off - 7));
+                        x1 = off <= 7 ? (kw1[wi] << (7 - off)) : (kw1[wi] >> (off - 7));
                     } else {
-                        x0 = __funnelshift_r(kw0[wi], kw0[wi + 1], off - 8);
-                        x1 = __funnelshift_r(kw1[wi], kw1[wi + 1], off - 8);
+                        x0 = __funnelshift_r(kw0[wi], kw0[wi + 1], off - 7);
+                        x1 = __funnelshift_r(kw1[wi], kw1[wi + 1], off - 7);
                     }
-                    const uint2 t0 = *reinterpret_cast<const uint2*>(lut + ((x0 & 0x3F00u) | lane8));
-                    const uint2 t1 = *reinterpret_cast<const uint2*>(lut + ((x1 & 0x3F00u) | lane8));
-                    af[2 * e] = t0.x;
-                    af[2 * e + 1] = t1.x;
-                    if constexpr (NC) {
-                        nsq[0] += __uint_as_float(t0.y);
-                        nsq[1] += __uint_as_float(t1.y);
-                    }
-                }
-            } else if constexpr (KB == 4) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int bit = 8 * (2 * j + e);
-                    const int wi = bit / 32, off = bit % 32;
-                    const uint32_t x0 = off <= 7 ? (kw0[wi] << (7 - off)) : (kw0[wi] >> (off - 7));
-                    const uint32_t x1 = off <= 7 ? (kw1[wi] << (7 - off)) : (kw1[wi] >> (off - 7));
-                    af[2 * e] = ld32(lut + ((x0 & 0x7F80u) | lane4));
-                    af[2 * e + 1] = ld32(lut + ((x1 & 0x7F80u) | lane4));
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int bit = 16 * (2 * j + e);
-                    const int wi = bit / 32, off = bit % 32;
-                    const __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
-                        static_cast<__nv_fp8x2_storage_t>((kw0[wi] >> off) & 0xffffu), __NV_E4M3);
-                    const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(
-                        static_cast<__nv_fp8x2_storage_t>((kw1[wi] >> off) & 0xffffu), __NV_E4M3);
-                    af[2 * e] = static_cast<uint32_t>(h0.x) | (static_cast<uint32_t>(h0.y) << 16);
-                    af[2 * e + 1] = static_cast<uint32_t>(h1.x) | (static_cast<uint32_t>(h1.y) << 16);
+                    af[2 * e] = ld32(lut + ((x0 & kIdx) | lane4));
+                    af[2 * e + 1] = ld32(lut + ((x1 & kIdx) | lane4));
                 }
             }
             const uint32_t afrag[4] = {af[0], af[1], af[2], af[3]};
-            const uint4 qb = qfrag[j * qstride];
-            mma16816(qacc[0], afrag, qb.x, qb.y);
-            mma16816(qacc[1], afrag, qb.z, qb.w);
-            if constexpr (NC && KB == 4) {
+            if constexpr (PACKQ) {
+                const uint2 qb = qfrag2[j * 32];
+                mma16816(qacc[j & 1], afrag, qb.x, qb.y);
+            } else {
+                const uint4 qb = qfrag[j * qstride];
+                mma16816(qacc[0], afrag, qb.x, qb.y);
+                mma16816(qacc[1], afrag, qb.z, qb.w);
+            }
+            if constexpr (NC) {
                 uint32_t sq[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -492,13 +561,14 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         float sacc[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[e] = qacc[0][e] + qacc[1][e];
+        if constexpr (PACKQ) {
+            // column n + 4 holds the lo part of column n: lanes c and c ^ 2 swap
+            // them, so columns n and n + 4 both end with the full score
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[e] += __shfl_xor_sync(kFull, sacc[e], 2);
+        }
         float n0 = 0.f, n1 = 0.f;  // ||c~||^2 of tokens r, r + 8 (this warp's share)
-        if constexpr (NC && KB == 3) {
-            n0 = nsq[0] + __shfl_xor_sync(kFull, nsq[0], 1);
-            n0 += __shfl_xor_sync(kFull, n0, 2);
-            n1 = nsq[1] + __shfl_xor_sync(kFull, nsq[1], 1);
-            n1 += __shfl_xor_sync(kFull, n1, 2);
-        } else if constexpr (NC && KB == 4) {
+        if constexpr (NC) {
             n0 = nacc[0];
             n1 = nacc[2];
         }
@@ -526,15 +596,15 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         // per-token factors: vec_norm, norm correction
         float f_r = 1.f, f_r8 = 1.f;
         if constexpr (KB != 8) {
-            f_r = half_from_bits(ld16(stage + n_off));
-            f_r8 = half_from_bits(ld16(stage + n_off + 8 * ROW));
+            f_r = half_from_bits(ld16(stage + n_off0));
+            f_r8 = half_from_bits(ld16(stage + n_off1));
             if constexpr (NC) {
                 f_r *= rsqrtf(n0);
                 f_r8 *= rsqrtf(n1);
             }
         }
-        const bool v_r = ok && tok0 + r < L;
-        const bool v_r8 = ok && tok0 + r + 8 < L;
+        const bool v_r = ok && tok0 + tq0 < L;
+        const bool v_r8 = ok && tok0 + tq1 < L;
         sc[0] = v_r ? sacc[0] * f_r : -INFINITY;
         sc[1] = v_r ? sacc[1] * f_r : -INFINITY;
         sc[2] = v_r8 ? sacc[2] * f_r8 : -INFINITY;
@@ -544,17 +614,26 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     // ---- value codes and (scale, zero) of one staged chunk, kept in registers
     // until the chunk's P.V one step later ------------------------------------------
     struct VRegs {
-        uint32_t w0[G::VWORDS], w1[G::VWORDS], w8[G::VWORDS], w9[G::VWORDS];  // tokens 2c, 2c+1, 2c+8, 2c+9
-        uint32_t sz0, sz1;  // half2 (scale, zero) of tokens r, r + 8
+        uint32_t w0[G::VREGS], w1[G::VREGS], w8[G::VREGS], w9[G::VREGS];  // k-columns 2c, 2c+1, 2c+8, 2c+9
+        uint32_t sz0, sz1;  // half2 (scale, zero) of rows r, r + 8
     };
     auto load_v = [&](const uint8_t* stage, VRegs& vr) {
-        ld_words(stage + v_off, vr.w0);
-        ld_words(stage + v_off + ROW, vr.w1);
-        ld_words(stage + v_off + 8 * ROW, vr.w8);
-        ld_words(stage + v_off + 9 * ROW, vr.w9);
-        vr.sz0 = static_cast<uint32_t>(ld16(stage + z_off)) | (static_cast<uint32_t>(ld16(stage + z_off + 2)) << 16);
-        vr.sz1 = static_cast<uint32_t>(ld16(stage + z_off + 8 * ROW)) |
-                 (static_cast<uint32_t>(ld16(stage + z_off + 8 * ROW + 2)) << 16);
+        if constexpr (G::VUNITS) {
+#pragma unroll
+            for (int m = 0; m < G::VNU; ++m) {
+                vr.w0[m] = ld_unit<G::VUNIT>(stage + v_off0 + 8 * G::VUNIT * m);
+                vr.w1[m] = ld_unit<G::VUNIT>(stage + v_off1 + 8 * G::VUNIT * m);
+                vr.w8[m] = ld_unit<G::VUNIT>(stage + v_off8 + 8 * G::VUNIT * m);
+                vr.w9[m] = ld_unit<G::VUNIT>(stage + v_off9 + 8 * G::VUNIT * m);
+            }
+        } else {
+            ld_words(stage, v_off0, vr.w0);
+            ld_words(stage, v_off1, vr.w1);
+            ld_words(stage, v_off8, vr.w8);
+            ld_words(stage, v_off9, vr.w9);
+        }
+        vr.sz0 = static_cast<uint32_t>(ld16(stage + z_off0)) | (static_cast<uint32_t>(ld16(stage + z_off0 + 2)) << 16);
+        vr.sz1 = static_cast<uint32_t>(ld16(stage + z_off1)) | (static_cast<uint32_t>(ld16(stage + z_off1 + 2)) << 16);
     };
 
     // ---- running state ---------------------------------------------------------------
@@ -621,8 +700,8 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         l_acc[1] += pr[1] + pr[3];
 
         // value scale / zero of tokens r and r + 8 (0 past the end)
-        const bool v_r = ok && tok0 + r < L;
-        const bool v_r8 = ok && tok0 + r + 8 < L;
+        const bool v_r = ok && tok0 + tq0 < L;
+        const bool v_r8 = ok && tok0 + tq1 < L;
         const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&vr.sz0));
         const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&vr.sz1));
         const float vs_r = v_r ? f0.x : 0.f, vz_r = v_r ? f0.y : 0.f;
@@ -640,10 +719,19 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 #pragma unroll
         for (int mt = 0; mt < G::MTILES; ++mt) {
             uint32_t vf[4];
-            vf[0] = value_sub<VB>(vr.w0, vr.w1, 2 * mt);
-            vf[1] = value_sub<VB>(vr.w0, vr.w1, 2 * mt + 1);
-            vf[2] = value_sub<VB>(vr.w8, vr.w9, 2 * mt);
-            vf[3] = value_sub<VB>(vr.w8, vr.w9, 2 * mt + 1);
+            if constexpr (G::VUNITS) {
+                // local dims 2mt, 2mt + 1 share one byte of unit m
+                const int m = (2 * mt) / G::VDPU, w = (2 * mt) % G::VDPU;
+                vf[0] = value_unit_sub(vr.w0[m], vr.w1[m], w);
+                vf[1] = value_unit_sub(vr.w0[m], vr.w1[m], w + 1);
+                vf[2] = value_unit_sub(vr.w8[m], vr.w9[m], w);
+                vf[3] = value_unit_sub(vr.w8[m], vr.w9[m], w + 1);
+            } else {
+                vf[0] = value_sub<VB>(vr.w0, vr.w1, 2 * mt);
+                vf[1] = value_sub<VB>(vr.w0, vr.w1, 2 * mt + 1);
+                vf[2] = value_sub<VB>(vr.w8, vr.w9, 2 * mt);
+                vf[3] = value_sub<VB>(vr.w8, vr.w9, 2 * mt + 1);
+            }
             mma16816(o[mt], vf, pb0, pb1);
         }
         mma16816(ob, a_bias, pb0, pb1);
@@ -676,16 +764,23 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
             }
         }
     };
+    // With a deep ring the stage of chunk it - 1 stays resident until its P.V
+    // (value codes re-read from shared memory); with a shallow one the codes
+    // ride in registers and the stage is released right after its QK.
+    constexpr bool kCarry = NS <= 3;
     float sc_prev[4];
     VRegs v_prev;
     bool ok_prev = false;
+    const uint8_t* stage_prev = ring;
     if (nch > 0) {
         int blk = -1;
-        const uint8_t* stage = acquire(0, blk);
+        stage_prev = acquire(0, blk);
         ok_prev = blk >= 0;
-        qk(stage, c0 * kTok, ok_prev, 0, sc_prev);
-        load_v(stage, v_prev);
-        release(0);
+        qk(stage_prev, c0 * kTok, ok_prev, 0, sc_prev);
+        if constexpr (kCarry) {
+            load_v(stage_prev, v_prev);
+            release(0);
+        }
     }
 #pragma unroll 1
     for (int it = 1; it < nch; ++it) {
@@ -695,20 +790,29 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         rescale(sc_prev);
         const bool ok = blk >= 0;
         float sc_cur[4];
-        VRegs v_cur;
         qk(stage, (c0 + it) * kTok, ok, it & 1, sc_cur);
-        load_v(stage, v_cur);
-        softmax_pv(sc_prev, v_prev, (c0 + it - 1) * kTok, ok_prev);
-        release(it);
+        if constexpr (kCarry) {
+            VRegs v_cur;
+            load_v(stage, v_cur);
+            softmax_pv(sc_prev, v_prev, (c0 + it - 1) * kTok, ok_prev);
+            release(it);
+            v_prev = v_cur;
+        } else {
+            load_v(stage_prev, v_prev);
+            softmax_pv(sc_prev, v_prev, (c0 + it - 1) * kTok, ok_prev);
+            release(it - 1);
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc_prev[e] = sc_cur[e];
-        v_prev = v_cur;
         ok_prev = ok;
+        stage_prev = stage;
     }
     if (nch > 0) {
         if (!ok_prev && !timed_out && lane == 0 && warp == 0) set_flag(c.flags, kFlagBlock);
         rescale(sc_prev);
+        if constexpr (!kCarry) load_v(stage_prev, v_prev);
         softmax_pv(sc_prev, v_prev, (c1 - 1) * kTok, ok_prev);
+        if constexpr (!kCarry) release(nch - 1);
     }
     if (timed_out) {
         if (lane == 0) {
@@ -749,9 +853,20 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 #pragma unroll
         for (int mt = 0; mt < G::MTILES; ++mt) {
             // sum P'(code - centre) = o * 2^(24 - pos) - centre * bias
-            const int d0 = r * (D / 8) + 2 * (part * G::MTILES + mt);
-            part_out[2 + d0] = fmaf(o[mt][e], value_weight<VB>(2 * mt), -cb) + z;
-            part_out[2 + d0 + 1] = fmaf(o[mt][2 + e], value_weight<VB>(2 * mt + 1), -cb) + z;
+            int d0;
+            float w0, w1;
+            if constexpr (G::VUNITS) {
+                const int m = (2 * mt) / G::VDPU, w = (2 * mt) % G::VDPU;
+                d0 = part * (D / WPH) + G::VDPU * (r + 8 * m) + w;
+                w0 = 16777216.f;  // even dim of the pair: low nibble
+                w1 = 1048576.f;   // odd dim: high nibble
+            } else {
+                d0 = r * (D / 8) + 2 * (part * G::MTILES + mt);
+                w0 = value_weight<VB>(2 * mt);
+                w1 = value_weight<VB>(2 * mt + 1);
+            }
+            part_out[2 + d0] = fmaf(o[mt][e], w0, -cb) + z;
+            part_out[2 + d0 + 1] = fmaf(o[mt][2 + e], w1, -cb) + z;
         }
     }
 }
@@ -771,7 +886,7 @@ constexpr int pick_wph(int want) {
 
 // Launch policy per shape: warps per head, resident CTAs per SM aimed for,
 // and the deepest stage ring that fits the shared memory that leaves.
-template <int D, int KB, int VB, int H>
+template <int D, int KB, int VB, int H, bool PACKQ>
 struct Policy {
     static constexpr int kWarpsTarget = 8;
     static constexpr int kWphRaw = kWarpsTarget / H;
@@ -779,18 +894,77 @@ struct Policy {
     static constexpr int WPH = pick_wph<D, KB, VB>(kWphRaw < 1 ? 1 : (kWphRaw > kWphMax ? kWphMax : kWphRaw));
     static constexpr int MINB = 32 * H * WPH > 256 ? 1 : 2;
     static constexpr int kBudget = MINB == 1 ? 220 * 1024 : 110 * 1024;
-    using G1 = Geo<D, KB, VB, H, WPH, 8>;
-    // fixed part plus the query fragments of up to 5 query heads per KV head
-    static constexpr int kFixed = G1::RING_OFF + 16 + H * 5 * D * 4;
+    using G1 = Geo<D, KB, VB, H, WPH, 8, PACKQ>;
+    // fixed part plus the query fragments (unpacked: up to 5 query heads per KV head)
+    static constexpr int kFixed = G1::RING_OFF + 16 + (PACKQ ? H * D * 16 : H * 5 * D * 4);
     static constexpr int kNs = (kBudget - kFixed) / G1::STAGE;
     static constexpr int NS = kNs < 2 ? 2 : (kNs > 8 ? 8 : kNs);
 };
 
-template <int D, int KB, int VB, bool NC, int H>
+// Shared-memory wavefronts one warp-wide load takes: the largest number of
+// distinct 4-byte words any bank is asked for (at least bytes / 128).
+inline int bank_wavefronts(const int (&addr)[32], int width) {
+    int words[32][8];
+    int count[32] = {};
+    int deg = 1;
+    for (int l = 0; l < 32; ++l) {
+        for (int wd = addr[l] / 4; wd <= (addr[l] + width - 1) / 4; ++wd) {
+            const int b = wd % 32;
+            bool seen = false;
+            for (int i = 0; i < count[b]; ++i) seen = seen || words[b][i] == wd;
+            if (!seen && count[b] < 8) words[b][count[b]++] = wd;
+            deg = count[b] > deg ? count[b] : deg;
+        }
+    }
+    const int floor = (width * 32 + 127) / 128;
+    return deg > floor ? deg : floor;
+}
+
+// Wavefronts of the code loads of one chunk, summed over the warps, under a
+// token order (eo: rows 0-7 take the even tokens and rows 8-15 the odd ones).
+// It mirrors the kernel's per-lane offsets.
+template <class G, int D, int KB, int VB, int H, int WPH>
+int load_wavefronts(bool eo) {
+    using S = typename G::S;
+    auto sig = [&](int k) { return eo ? (k < 8 ? 2 * k : 2 * (k - 8) + 1) : k; };
+    int total = 0;
+    int addr[32];
+    for (int h = 0; h < H; ++h) {
+        const int hs = h * G::SA;
+        for (int part = 0; part < WPH; ++part) {
+            for (int k = 0; k < 16; k += 8) {
+                for (int l = 0; l < 32; ++l) {
+                    const int r = l / 4, c = l % 4;
+                    const int base = G::KUNITS ? hs + part * G::KSH + G::KUNIT * c
+                                               : hs + c * G::KBYTES + part * G::KBYTES_W;
+                    addr[l] = sig(r + k) * G::ROW + base;
+                    if (!G::KUNITS) addr[l] &= ~3;
+                }
+                total += G::KUNITS ? bank_wavefronts(addr, G::KUNIT) * G::KSTEPS
+                                   : bank_wavefronts(addr, 4) * (G::KWORDS + 1);
+            }
+            const int kcols[4] = {0, 1, 8, 9};
+            for (int kc : kcols) {
+                for (int l = 0; l < 32; ++l) {
+                    const int r = l / 4, c = l % 4;
+                    const int base = G::VUNITS ? hs + S::kKeyBytes + part * G::VSH + G::VUNIT * r
+                                               : hs + S::kKeyBytes + (r * (D / 8) * VB + part * G::VBITS_W) / 8;
+                    addr[l] = sig(2 * c + kc) * G::ROW + base;
+                    if (!G::VUNITS) addr[l] &= ~3;
+                }
+                total += G::VUNITS ? bank_wavefronts(addr, G::VUNIT) * G::VNU
+                                   : bank_wavefronts(addr, 4) * (G::VWORDS + 1);
+            }
+        }
+    }
+    return total;
+}
+
+template <int D, int KB, int VB, bool NC, int H, bool PACKQ>
 struct Kernel {
-    using P = Policy<D, KB, VB, H>;
-    using G = Geo<D, KB, VB, H, P::WPH, P::NS>;
-    static constexpr auto fn = decode_kernel<D, KB, VB, NC, H, P::WPH, P::NS, P::MINB>;
+    using P = Policy<D, KB, VB, H, PACKQ>;
+    using G = Geo<D, KB, VB, H, P::WPH, P::NS, PACKQ>;
+    static constexpr auto fn = decode_kernel<D, KB, VB, NC, H, P::WPH, P::NS, P::MINB, PACKQ>;
 
     static cudaError_t prepare(int hq, int* smem) {
         *smem = G::smem_bytes(hq);
@@ -807,8 +981,12 @@ struct Kernel {
         int smem = 0;
         const cudaError_t e = prepare(a.num_q_heads, &smem);
         if (e != cudaSuccess) return e;
+        static const int tok_eo =
+            load_wavefronts<G, D, KB, VB, H, P::WPH>(true) < load_wavefronts<G, D, KB, VB, H, P::WPH>(false) ? 1 : 0;
+        Args args = a;
+        args.tok_eo = tok_eo;
         dim3 grid(static_cast<unsigned>(a.num_splits), static_cast<unsigned>(num_seqs));
-        fn<<<grid, G::NT, smem, stream>>>(p, c, a);
+        fn<<<grid, G::NT, smem, stream>>>(p, c, args);
         return cudaGetLastError();
     }
 };
@@ -822,14 +1000,21 @@ cudaError_t run(const LayerParams& p, const CacheGeom& c, const Args& a, int num
         if (ctas != nullptr) return K::occupancy(a.num_q_heads, ctas);
         return K::launch(p, c, a, num_seqs, stream);
     };
+    // up to 4 query heads per KV head: hi and lo query parts share one MMA
+    const bool packq = num_kv_heads > 0 && a.num_q_heads / num_kv_heads <= 4;
     auto by_h = [&](auto kb, auto vb, auto nc) -> cudaError_t {
         constexpr int KB = decltype(kb)::value, VB = decltype(vb)::value;
         constexpr bool NC = decltype(nc)::value;
+        auto by_q = [&](auto h) -> cudaError_t {
+            constexpr int HH = decltype(h)::value;
+            if (packq) return go(Kernel<D, KB, VB, NC, HH, true>{});
+            return go(Kernel<D, KB, VB, NC, HH, false>{});
+        };
         switch (num_kv_heads) {
-            case 1: return go(Kernel<D, KB, VB, NC, 1>{});
-            case 2: return go(Kernel<D, KB, VB, NC, 2>{});
-            case 4: return go(Kernel<D, KB, VB, NC, 4>{});
-            case 8: return go(Kernel<D, KB, VB, NC, 8>{});
+            case 1: return by_q(std::integral_constant<int, 1>{});
+            case 2: return by_q(std::integral_constant<int, 2>{});
+            case 4: return by_q(std::integral_constant<int, 4>{});
+            case 8: return by_q(std::integral_constant<int, 8>{});
             default: return cudaErrorInvalidValue;
         }
     };
