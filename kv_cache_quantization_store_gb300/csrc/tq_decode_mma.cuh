@@ -250,7 +250,7 @@ struct Geo {
     static constexpr int VREGS = VUNITS ? VNU : VWORDS;
     static constexpr int LUT_ENTRIES = KB == 3 ? 64 : (KB == 4 ? 256 : 0);
     static constexpr int LUT_BYTES = LUT_ENTRIES * 32 * 4;  // half2 per entry and lane
-    static constexpr int XCH_W = WPH > 1 ? 32 * 8 * 4 : 0;  // per warp and buffer
+    static constexpr int XCH_W = WPH > 1 ? 32 * 6 * 4 : 0;  // per warp and buffer: 32 x {4 scores, 2 norms}
     static constexpr int X_OFF = LUT_BYTES;
     // control block: full mbarrier, release counter, block id per stage; error word
     static constexpr int CTRL_OFF = X_OFF + 2 * NWARPS * XCH_W;
@@ -474,7 +474,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     const int v_off8 = sig(2 * cc + 8) * ROW + vbase, v_off9 = sig(2 * cc + 9) * ROW + vbase;
     const uint8_t* lut = smem;
     const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
-    float* xch = reinterpret_cast<float*>(smem + G::X_OFF);  // [buffer][warp][lane][8]
+    float* xch = reinterpret_cast<float*>(smem + G::X_OFF);  // [buffer][warp][32 float4 | 32 float2]
 
     // ---- QK of one staged chunk: log2-domain scores of tokens r, r + 8 for
     // query columns 2c, 2c + 1, -inf past the sequence end ---------------------------
@@ -574,23 +574,23 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         }
         if constexpr (WPH > 1) {
             // add the other warps' shares of the dims
-            float* xb = xch + buf * (G::NWARPS * 32 * 8);  // alternate buffers: no overwrite before it is read
-            float4* mine = reinterpret_cast<float4*>(xb + (warp * 32 + lane) * 8);
-            mine[0] = make_float4(sacc[0], sacc[1], sacc[2], sacc[3]);
-            mine[1] = make_float4(n0, n1, 0.f, 0.f);
+            float* xb = xch + buf * (G::NWARPS * 32 * 6);  // alternate buffers: no overwrite before it is read
+            reinterpret_cast<float4*>(xb + warp * 192)[lane] = make_float4(sacc[0], sacc[1], sacc[2], sacc[3]);
+            if constexpr (NC) reinterpret_cast<float2*>(xb + warp * 192 + 128)[lane] = make_float2(n0, n1);
             group_barrier(1 + h, 32 * WPH);
 #pragma unroll
             for (int w = 1; w < WPH; ++w) {
                 const int ow = h * WPH + (part + w) % WPH;
-                const float4* other = reinterpret_cast<const float4*>(xb + (ow * 32 + lane) * 8);
-                const float4 os = other[0];
-                const float4 on = other[1];
+                const float4 os = reinterpret_cast<const float4*>(xb + ow * 192)[lane];
                 sacc[0] += os.x;
                 sacc[1] += os.y;
                 sacc[2] += os.z;
                 sacc[3] += os.w;
-                n0 += on.x;
-                n1 += on.y;
+                if constexpr (NC) {
+                    const float2 on = reinterpret_cast<const float2*>(xb + ow * 192 + 128)[lane];
+                    n0 += on.x;
+                    n1 += on.y;
+                }
             }
         }
         // per-token factors: vec_norm, norm correction
@@ -893,7 +893,8 @@ struct Policy {
     static constexpr int kWphMax = D / 32;  // at least two k-steps per warp
     static constexpr int WPH = pick_wph<D, KB, VB>(kWphRaw < 1 ? 1 : (kWphRaw > kWphMax ? kWphMax : kWphRaw));
     static constexpr int MINB = 32 * H * WPH > 256 ? 1 : 2;
-    static constexpr int kBudget = MINB == 1 ? 220 * 1024 : 110 * 1024;
+    // per-CTA shared memory: 228 KB per SM, less 1 KB reserved per CTA
+    static constexpr int kBudget = MINB == 1 ? 227 * 1024 : 113 * 1024;
     using G1 = Geo<D, KB, VB, H, WPH, 8, PACKQ>;
     // fixed part plus the query fragments (unpacked: up to 5 query heads per KV head)
     static constexpr int kFixed = G1::RING_OFF + 16 + (PACKQ ? H * D * 16 : H * 5 * D * 4);
