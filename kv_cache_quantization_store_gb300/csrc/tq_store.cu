@@ -20,6 +20,47 @@ namespace {
 
 constexpr int kStoreWarps = 8;
 
+// Butterflies across the LPV lanes of one vector as fma(+-1, x, partner):
+// the same single rounding as the add or the subtract it stands for.
+template <int N, int LPV>
+__device__ __forceinline__ void fwht_lanes_fma(float (&x)[N], int part) {
+#pragma unroll
+    for (int m = 1; m < LPV; m <<= 1) {
+        const float sg = (part & m) ? -1.f : 1.f;
+#pragma unroll
+        for (int i = 0; i < N; ++i) x[i] = fmaf(sg, x[i], __shfl_xor_sync(kFull, x[i], m));
+    }
+}
+
+// Number of the positive decision thresholds t[0] < t[1] < ... below a >= 0
+// (strictly), by binary search over the 3 (3-bit) or 7 (4-bit) thresholds.
+template <int NT>
+__device__ __forceinline__ uint32_t count_above(float a, const float (&t)[NT]) {
+    static_assert(NT == 3 || NT == 7, "3 or 7 positive thresholds");
+    if constexpr (NT == 3) {
+        const bool p1 = a > t[1];
+        const bool p2 = a > (p1 ? t[2] : t[0]);
+        return (p1 ? 2u : 0u) + (p2 ? 1u : 0u);
+    } else {
+        const bool p1 = a > t[3];
+        const bool p2 = a > (p1 ? t[5] : t[1]);
+        const float tc = p1 ? (p2 ? t[6] : t[4]) : (p2 ? t[2] : t[0]);
+        const bool p3 = a > tc;
+        return (p1 ? 4u : 0u) + (p2 ? 2u : 0u) + (p3 ? 1u : 0u);
+    }
+}
+
+// Correctly rounded fp32 quotient a / s from y = RN(1 / s): q0 = RN(a y) is
+// within one ulp of a / s, the residual a - s q0 is exact in one fma, and
+// RN(q0 + r y) is the correctly rounded quotient (P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990), for finite a and finite non-zero s.
+__device__ __forceinline__ float quotient_rn(float a, float s, float y) {
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-s, q0, a);
+    return __fmaf_rn(r, y, q0);
+}
+
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(kStoreWarps * 32)
 store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict__ k,
@@ -33,6 +74,9 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     constexpr int kHalf = KB == 8 ? 2 : (1 << KB) / 2;  // levels per sign
 
     __shared__ __align__(16) uint8_t stage_all[kStoreWarps][VPW * SA + 2];
+    // per lane part: XOR masks that flip the sign bits of the bf16 pairs
+    // (elements 2j, 2j + 1 of the part) the random signs negate
+    __shared__ __align__(16) uint32_t sign_mask[LPV][EPL / 2];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     uint8_t* stage = stage_all[warp];
@@ -41,13 +85,18 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     const int H = c.num_kv_heads;
     const int64_t num_vecs = num_tokens * H;
 
-    // This lane's slice of the sign diagonal, and the positive-half decision
-    // thresholds (the grid is symmetric about 0 and the middle boundary is 0).
-    uint32_t signs = 0;
+    // Sign masks, and the positive-half decision thresholds (the grid is
+    // symmetric about 0 and the middle boundary is 0).
     float pos_b[kHalf - 1];
     if constexpr (KB != 8) {
-        const int first = part * EPL;
-        signs = p.sign_mask[first / 32] >> (first % 32);
+        for (int i = threadIdx.x; i < LPV * EPL / 2; i += kStoreWarps * 32) {
+            const int pp = i / (EPL / 2), j = i % (EPL / 2);
+            const int e = pp * EPL + 2 * j;
+            const uint32_t b0 = (p.sign_mask[e / 32] >> (e % 32)) & 1u;
+            const uint32_t b1 = (p.sign_mask[(e + 1) / 32] >> ((e + 1) % 32)) & 1u;
+            sign_mask[pp][j] = (b0 << 15) | (b1 << 31);
+        }
+        __syncthreads();
 #pragma unroll
         for (int j = 0; j < kHalf - 1; ++j) pos_b[j] = p.boundaries[kHalf + j];
     }
@@ -64,8 +113,8 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
         // ---- key -----------------------------------------------------------
         {
             float x[EPL];
-            load_bf16<EPL>(k + vsafe * D + part * EPL, x);
             if constexpr (KB == 8) {
+                load_bf16<EPL>(k + vsafe * D + part * EPL, x);
                 // FP8 e4m3, round to nearest even, saturating finite.
                 uint32_t w[EPL / 4];
 #pragma unroll
@@ -78,16 +127,27 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                 }
                 write_u16_words(my_slot + part * EPL, EPL, w);
             } else {
-                float ss = 0.f;
+                // bf16 pairs with the random signs applied to the raw sign bits
+                const uint4* src = reinterpret_cast<const uint4*>(k + vsafe * D + part * EPL);
+                const uint4* msk = reinterpret_cast<const uint4*>(sign_mask[part]);
+#pragma unroll
+                for (int j = 0; j < EPL / 8; ++j) {
+                    const uint4 u = __ldg(src + j);
+                    const uint4 m = msk[j];
+                    const uint32_t w[4] = {u.x ^ m.x, u.y ^ m.y, u.z ^ m.z, u.w ^ m.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        x[8 * j + 2 * q] = bf16_lo(w[q]);
+                        x[8 * j + 2 * q + 1] = bf16_hi(w[q]);
+                    }
+                }
+                float ss = 0.f;  // the signs do not change the squares
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) ss = fmaf(x[i], x[i], ss);
                 ss = sum_lanes<LPV>(ss);
                 const float n = sqrtf(ss);
-#pragma unroll
-                for (int i = 0; i < EPL; ++i)
-                    if ((signs >> i) & 1u) x[i] = -x[i];
                 fwht_local<EPL>(x);
-                fwht_lanes<EPL, LPV>(x, part);
+                fwht_lanes_fma<EPL, LPV>(x, part);
                 // x = sqrt(d) * n * y with y = Pi k / n; compare against the
                 // boundaries scaled the same way.
                 const float u = n * sqrt_d;
@@ -97,10 +157,7 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                 uint32_t code[EPL];
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) {
-                    const float a = fabsf(x[i]);
-                    uint32_t cnt = 0;
-#pragma unroll
-                    for (int j = 0; j < kHalf - 1; ++j) cnt += (a > t[j]) ? 1u : 0u;
+                    const uint32_t cnt = count_above(fabsf(x[i]), t);
                     code[i] = x[i] > 0.f ? kHalf + cnt : kHalf - 1 - cnt;
                 }
                 uint32_t w[(EPL * KB + 31) / 32];
@@ -128,11 +185,23 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
             const float s = half_from_bits(sb);
             const float z = half_from_bits(zb);
             uint32_t code[EPL];
+            if (isfinite(mn) && isfinite(mx) && isfinite(z) && isfinite(s)) {
+                // y = 0 for a zero scale gives quotient 0, i.e. code 0
+                const float y = (s == 0.f) ? 0.f : __frcp_rn(s);
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                const float qv = __fdiv_rn(__fsub_rn(x[i], z), s);
-                const float r = fminf(fmaxf(rintf(qv), 0.f), static_cast<float>(kTopV));
-                code[i] = (s == 0.f) ? 0u : static_cast<uint32_t>(r);
+                for (int i = 0; i < EPL; ++i) {
+                    const float qv = quotient_rn(__fsub_rn(x[i], z), s, y);
+                    // clamp, then round half to even by the 1.5 * 2^23 addition
+                    const float c = fminf(fmaxf(qv, 0.f), static_cast<float>(kTopV));
+                    code[i] = __float_as_uint(__fadd_rn(c, 12582912.f)) & static_cast<uint32_t>(kTopV);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) {
+                    const float qv = __fdiv_rn(__fsub_rn(x[i], z), s);
+                    const float r = fminf(fmaxf(rintf(qv), 0.f), static_cast<float>(kTopV));
+                    code[i] = (s == 0.f) ? 0u : static_cast<uint32_t>(r);
+                }
             }
             uint32_t w[(EPL * VB + 31) / 32];
             pack_codes<EPL, VB>(code, w);

@@ -205,3 +205,53 @@ def test_empty_inputs(cuda_device):
     assert not cache.data.any()
     out = gpu_decode(wl, cfg, cache, wl.q(), cuda_device, seq_lens=[0])
     assert np.all(out == 0)
+
+
+def _bf16_round(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def _bf16_step(x, steps):
+    """x (bf16-representable) moved by `steps` bf16 ulps away from zero; values
+    within 2 ulps of zero stay put (no step across zero into NaN patterns)."""
+    b = torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    steps = np.where((b.astype(np.int32) & 0x7FFF) > 2, np.asarray(steps, dtype=np.int32), 0)
+    b = (b.astype(np.int32) + steps).astype(np.int16)
+    return torch.from_numpy(b).view(torch.bfloat16).float().numpy()
+
+
+@pytest.mark.parametrize("vb", [3, 4])
+def test_value_codes_at_quotient_ties(cuda_device, vb):
+    """Value codes where (v - zero) / scale sits at, or a few bf16 steps from,
+    a rounding tie k + 1/2, over thousands of scales; plus a zero scale, a
+    zero point past the fp16 range and a scale past it.  Value bytes must
+    equal the oracle's (IEEE fp32 division, rint half to even)."""
+    d, n_tok = 64, 4096
+    top = (1 << vb) - 1
+    wl = W.custom(d, 3, vb, False, 1, 1, 16, [n_tok], 2600 + vb)
+    rng = np.random.default_rng(2610 + vb)
+    k, _ = wl.kv()
+    v = np.empty((n_tok, 1, d), dtype=np.float32)
+    lo = _bf16_round(-rng.uniform(0.05, 8, n_tok) * 10.0 ** rng.uniform(-3, 3, n_tok))
+    hi = _bf16_round(lo + np.abs(lo) * rng.uniform(0.02, 4, n_tok))
+    s = ((hi - lo).astype(np.float32) / np.float32(top)).astype(np.float16).astype(np.float32)
+    z = lo.astype(np.float16).astype(np.float32)
+    kk = rng.integers(0, top, (n_tok, d - 2)) + 0.5
+    target = _bf16_round(z[:, None] + s[:, None] * kk)
+    v[:, 0, 0], v[:, 0, 1] = lo, hi
+    v[:, 0, 2:] = _bf16_step(target, rng.integers(-2, 3, target.shape))
+    v[:, 0, 2:] = np.clip(v[:, 0, 2:], lo[:, None], hi[:, None])
+    v[0, 0, :] = 1.25                                  # zero scale
+    v[1, 0, :] = _bf16_round(rng.uniform(-2, 2, d))
+    v[1, 0, 0] = -70000.0                              # zero point beyond fp16: IEEE path
+    v[2, 0, :] = _bf16_round(rng.uniform(-1e4, 2e6, d))
+    v[2, 0, 0], v[2, 0, 1] = -1.0e4, 2.0e6             # scale beyond fp16
+    v = _bf16_round(v)
+    assert np.all(np.isfinite(v))
+    cfg, cache = gpu_store(wl, 0, cuda_device, k, v)
+    layer = oracle_layer(wl, 0)
+    ocache, near = oracle_cache(wl, layer, k, v)
+    sm = wl.slot_mapping()
+    got = slot_bytes(cache.data.cpu().numpy(), wl, cfg.slot_size_aligned, sm).reshape(-1, cfg.slot_size_aligned)
+    want = slot_bytes(ocache.data, wl, cfg.slot_size_aligned, sm).reshape(-1, cfg.slot_size_aligned)
+    compare_slots(layer, got, want, near.reshape(-1, d), k.reshape(-1, d))
