@@ -135,6 +135,16 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def decode_source_digest() -> str:
+    """sha256 (16 hex digits) over the decode kernel sources, in name order."""
+    csrc = ROOT / "kv_cache_quantization_store_gb300" / "csrc"
+    h = hashlib.sha256()
+    for f in sorted(csrc.glob("tq_decode*")):
+        h.update(f.name.encode())
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
 def decode_traffic_record():
     """DRAM bytes per decode launch from the committed ncu summary, used only
     while the decode source is unchanged since the capture (else None)."""
@@ -146,9 +156,7 @@ def decode_traffic_record():
         if "=" in line and not line.lstrip().startswith("#"):
             key, val = line.split("=", 1)
             vals[key.strip()] = val.strip()
-    src = ROOT / "kv_cache_quantization_store_gb300" / "csrc" / "tq_decode.cu"
-    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
-    if vals.get("source_sha256_16") != digest:
+    if vals.get("source_sha256_16") != decode_source_digest():
         return None
     try:
         return float(vals["dram_bytes_per_launch_c4"])
