@@ -255,7 +255,10 @@ struct Geo {
     // control block: full mbarrier, release counter, block id per stage; error word
     static constexpr int CTRL_OFF = X_OFF + 2 * NWARPS * XCH_W;
     static constexpr int CTRL_BYTES = (16 * NS + 16 + 15) & ~15;
-    static constexpr int ZERO_OFF = CTRL_OFF + CTRL_BYTES;
+    // the split's block-table entries (the first BT_MAX; later ones are read from global)
+    static constexpr int BT_MAX = 512;
+    static constexpr int BT_OFF = CTRL_OFF + CTRL_BYTES;
+    static constexpr int ZERO_OFF = BT_OFF + 4 * BT_MAX;
     static constexpr int RING_OFF = ZERO_OFF + 16;
     static constexpr int RING = NS * STAGE + 16;
     // Q' fragments follow the ring.  PACKQ (G <= 4): per warp and k-step one
@@ -306,6 +309,16 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     const int n_chunks = (L + kTok - 1) / kTok;
     const int c0 = split * a.chunks_per_split;
     const int c1 = min(c0 + a.chunks_per_split, n_chunks);
+
+    // ---- this split's block-table entries, staged once -------------------------------
+    {
+        const int cpb_ = c.block_size / kTok;
+        const int first = c0 / cpb_;
+        const int n_bt = c1 > c0 ? min((c1 - 1) / cpb_ - first + 1, G::BT_MAX) : 0;
+        const int32_t* row = a.block_table + static_cast<int64_t>(s) * a.max_blocks + first;
+        int* dst = reinterpret_cast<int*>(smem + G::BT_OFF);
+        for (int i = threadIdx.x; i < n_bt; i += NT) dst[i] = row[i];
+    }
 
     // ---- control block: stage mbarriers and counters ------------------------------
     if (threadIdx.x == 0) {
@@ -435,11 +448,13 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     const int cpb = c.block_size / kTok;  // 16-token chunks per paged block
     const int32_t* bt_row = a.block_table + static_cast<int64_t>(s) * a.max_blocks;
     const int nch = c1 - c0;
+    const int col0 = c0 / cpb;
+    const int* bt_sm = reinterpret_cast<const int*>(smem + G::BT_OFF);
     auto issue = [&](int it) {  // one thread
         const int slot = it % NS;
         const int cg = c0 + it;
         const int col = cg / cpb;
-        int b = bt_row[col];
+        int b = col - col0 < G::BT_MAX ? bt_sm[col - col0] : bt_row[col];
         b = (b >= 0 && b < c.num_blocks) ? b : -1;
         stage_blk[slot] = b;
         if (b >= 0) {
@@ -567,7 +582,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) sacc[e] += __shfl_xor_sync(kFull, sacc[e], 2);
         }
-        float n0 = 0.f, n1 = 0.f;  // ||c~||^2 of tokens r, r + 8 (this warp's share)
+        float n0 = 0.f, n1 = 0.f;  // ||c~||^2 of rows r, r + 8 (this warp's share)
         if constexpr (NC) {
             n0 = nacc[0];
             n1 = nacc[2];
@@ -643,7 +658,10 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
     float ob[4] = {0.f, 0.f, 0.f, 0.f};  // row 0: sum of P' per query column
-    float m_ref[2] = {-INFINITY, -INFINITY};
+    // A finite start (far below any score) keeps every exponent and rescale
+    // factor finite: the first chunk always raises it to the real maximum.
+    constexpr float kMinRef = -1e30f;
+    float m_ref[2] = {kMinRef, kMinRef};
     float l_acc[2] = {0.f, 0.f};
     float z_acc[2] = {0.f, 0.f};
     const uint32_t bias_a = (r == 0) ? 0x3C003C00u : 0u;
@@ -665,8 +683,8 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
             }
             const float n0m = fmaxf(m_ref[0], mx0);
             const float n1m = fmaxf(m_ref[1], mx1);
-            const float al0 = (n0m == -INFINITY) ? 1.f : fast_exp2(m_ref[0] - n0m);
-            const float al1 = (n1m == -INFINITY) ? 1.f : fast_exp2(m_ref[1] - n1m);
+            const float al0 = fast_exp2(m_ref[0] - n0m);
+            const float al1 = fast_exp2(m_ref[1] - n1m);
 #pragma unroll
             for (int mt = 0; mt < G::MTILES; ++mt) {
                 o[mt][0] *= al0;
@@ -687,15 +705,13 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         }
     };
     auto softmax_pv = [&](const float (&sc)[4], const VRegs& vr, int tok0, bool ok) {
-        // After the rescale test every column's reference max is finite or all its
-        // scores are -inf; exp2(-inf) = 0 masks past-the-end tokens.
+        // After the rescale test every finite score is at most 2^8 above its
+        // column's reference; exp2(-inf) = 0 masks past-the-end tokens.
         float pr[4];
         pr[0] = fast_exp2(sc[0] - m_ref[0]);
         pr[1] = fast_exp2(sc[1] - m_ref[1]);
         pr[2] = fast_exp2(sc[2] - m_ref[0]);
         pr[3] = fast_exp2(sc[3] - m_ref[1]);
-        if (m_ref[0] == -INFINITY) pr[0] = pr[2] = 0.f;
-        if (m_ref[1] == -INFINITY) pr[1] = pr[3] = 0.f;
         l_acc[0] += pr[0] + pr[2];
         l_acc[1] += pr[1] + pr[3];
 
