@@ -70,48 +70,6 @@ struct Args {
     int tok_eo;       // token order of the chunk rows: 0 natural, 1 even tokens then odd tokens
 };
 
-// One-dimensional bulk copy global -> shared that signals completion on an
-// mbarrier of this CTA (complete_tx of `bytes`).
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(mbar)
-        : "memory");
-}
-__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(mbar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(uint32_t mbar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(mbar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Waits for phase `parity` of an mbarrier, giving up after about a second.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
-    if (mbar_try_wait(mbar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(mbar, parity))
-        if (clock64() - t0 > (1ll << 31)) return false;
-    return true;
-}
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
-// Shared-memory counter increment with acquire-release ordering; returns the old value.
-__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t addr, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(addr), "r"(v) : "memory");
-    return old;
-}
-
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -330,6 +288,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
             reinterpret_cast<int*>(ctl + 12 * NS)[st] = -1;
         }
         *reinterpret_cast<int*>(ctl + 16 * NS) = 0;
+        fence_mbar_init();
     }
 
     // ---- pair lookup table: centroids * lut_scale as fp16, one copy per lane ----

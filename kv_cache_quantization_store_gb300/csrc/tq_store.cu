@@ -61,6 +61,31 @@ __device__ __forceinline__ float quotient_rn(float a, float s, float y) {
     return __fmaf_rn(r, y, q0);
 }
 
+// Writes the NB low-order bytes of `bits` (NB = 3, 4 or 8) at a byte address of
+// shared memory; `two_aligned` says the address is even.
+template <int NB>
+__device__ __forceinline__ void put_bytes(uint8_t* dst, uint64_t bits, bool two_aligned) {
+    if constexpr (NB == 3) {
+        dst[0] = static_cast<uint8_t>(bits);
+        dst[1] = static_cast<uint8_t>(bits >> 8);
+        dst[2] = static_cast<uint8_t>(bits >> 16);
+    } else {
+        (void)two_aligned;  // 4- and 8-byte groups start on even offsets
+        uint16_t* h = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+        for (int i = 0; i < NB / 2; ++i) h[i] = static_cast<uint16_t>(bits >> (16 * i));
+    }
+}
+
+// Packs 8 codes of B bits LSB-first.
+template <int B>
+__device__ __forceinline__ uint64_t pack8(const uint32_t* code) {
+    uint64_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w |= static_cast<uint64_t>(code[e]) << (B * e);
+    return w;
+}
+
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(kStoreWarps * 32)
 store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict__ k,
@@ -72,11 +97,26 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     constexpr int SA = S::kAligned;
     constexpr int kTopV = (1 << VB) - 1;
     constexpr int kHalf = KB == 8 ? 2 : (1 << KB) / 2;  // levels per sign
+    constexpr int kSpan = VPW * D;                      // bf16 elements of one warp step (K or V)
+    // MSE keys (arithmetic-heavy) stage the next step's K and V rows in
+    // shared memory by bulk copies; FP8 keys (little arithmetic) read them
+    // straight from global memory, coalesced 128 bytes per quarter-warp.
+    constexpr bool kPrefetch = KB != 8;
 
+    // Element layout: lane part p of a vector owns elements 8 (p + LPV j) + e
+    // (j < EPL / 8, e < 8) as x[8 j + e].  The Walsh-Hadamard transform
+    // factors over the index bits, so the in-register stages cover bits
+    // 0-2 and the bits above the lane bits, and the shuffle stages the lane
+    // bits.  Each 8-element group is 16 contiguous bf16 bytes (the 8 lanes of
+    // a quarter-warp read 128 contiguous bytes) and packs to whole bytes.
     __shared__ __align__(16) uint8_t stage_all[kStoreWarps][VPW * SA + 2];
-    // per lane part: XOR masks that flip the sign bits of the bf16 pairs
-    // (elements 2j, 2j + 1 of the part) the random signs negate
+    // per lane part: XOR masks that flip the sign bits of the bf16 pairs the
+    // random signs negate, word w of group j at [4 j + w]
     __shared__ __align__(16) uint32_t sign_mask[LPV][EPL / 2];
+    // K and V rows of the warp's next step, prefetched by bulk copies
+    extern __shared__ __align__(16) uint8_t kv_ring[];  // [warp][slot][K | V][kSpan] bf16
+    __shared__ __align__(8) uint64_t kv_full[kStoreWarps][2];
+
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     uint8_t* stage = stage_all[warp];
@@ -90,49 +130,92 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     float pos_b[kHalf - 1];
     if constexpr (KB != 8) {
         for (int i = threadIdx.x; i < LPV * EPL / 2; i += kStoreWarps * 32) {
-            const int pp = i / (EPL / 2), j = i % (EPL / 2);
-            const int e = pp * EPL + 2 * j;
+            const int pp = i / (EPL / 2), jw = i % (EPL / 2);
+            const int e = 8 * (pp + LPV * (jw / 4)) + 2 * (jw % 4);
             const uint32_t b0 = (p.sign_mask[e / 32] >> (e % 32)) & 1u;
             const uint32_t b1 = (p.sign_mask[(e + 1) / 32] >> ((e + 1) % 32)) & 1u;
-            sign_mask[pp][j] = (b0 << 15) | (b1 << 31);
+            sign_mask[pp][jw] = (b0 << 15) | (b1 << 31);
         }
-        __syncthreads();
 #pragma unroll
         for (int j = 0; j < kHalf - 1; ++j) pos_b[j] = p.boundaries[kHalf + j];
     }
+    if (kPrefetch && threadIdx.x == 0) {
+        for (int w = 0; w < kStoreWarps; ++w) {
+            mbar_init(static_cast<uint32_t>(__cvta_generic_to_shared(&kv_full[w][0])), 1u);
+            mbar_init(static_cast<uint32_t>(__cvta_generic_to_shared(&kv_full[w][1])), 1u);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
     const float sqrt_d = sqrtf(static_cast<float>(D));
 
+    const uint16_t* ring = reinterpret_cast<const uint16_t*>(kv_ring) + warp * 4 * kSpan;
+    const uint32_t ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    const uint32_t full_sh = static_cast<uint32_t>(__cvta_generic_to_shared(&kv_full[warp][0]));
+    // lane 0: stage the K and V rows of the VPW vectors from `b` into slot sl
+    auto issue = [&](int64_t b, int sl) {
+        const int64_t n = num_vecs - b < VPW ? num_vecs - b : VPW;
+        const uint32_t bytes = static_cast<uint32_t>(n) * D * 2;
+        mbar_arrive_tx(full_sh + 8u * sl, 2u * bytes);
+        bulk_copy(ring_sh + static_cast<uint32_t>(2 * sl) * kSpan * 2, k + b * D, bytes, full_sh + 8u * sl);
+        bulk_copy(ring_sh + static_cast<uint32_t>(2 * sl + 1) * kSpan * 2, v + b * D, bytes, full_sh + 8u * sl);
+    };
+
     const int64_t step = static_cast<int64_t>(gridDim.x) * kStoreWarps * VPW;
-    for (int64_t base = (static_cast<int64_t>(blockIdx.x) * kStoreWarps + warp) * VPW; base < num_vecs;
-         base += step) {
+    int64_t base = (static_cast<int64_t>(blockIdx.x) * kStoreWarps + warp) * VPW;
+    if (kPrefetch && lane == 0 && base < num_vecs) issue(base, 0);
+    bool timed_out = false;
+    int it = 0;
+    for (; base < num_vecs; base += step, ++it) {
+        const int sl = it & 1;
+        if constexpr (kPrefetch) {
+            if (lane == 0 && base + step < num_vecs) {
+                fence_proxy_async();  // the other slot was read through the generic proxy
+                issue(base + step, sl ^ 1);
+            }
+            if (!mbar_wait(full_sh + 8u * sl, static_cast<uint32_t>((it >> 1) & 1))) {
+                timed_out = true;
+                break;
+            }
+        }
         const int64_t vi = base + vin;
         const bool valid = vi < num_vecs;
         const int64_t vsafe = valid ? vi : num_vecs - 1;
         uint8_t* my_slot = stage + vin * SA;
+        // this lane's groups: 16 bytes at element 8 (part + LPV j) of its vector
+        const uint4* ksrc = kPrefetch ? reinterpret_cast<const uint4*>(ring + 2 * sl * kSpan + vin * D) + part
+                                      : reinterpret_cast<const uint4*>(k + vsafe * D) + part;
+        const uint4* vsrc = kPrefetch ? reinterpret_cast<const uint4*>(ring + (2 * sl + 1) * kSpan + vin * D) + part
+                                      : reinterpret_cast<const uint4*>(v + vsafe * D) + part;
+        // 16-byte group j of K or V: shared memory (staged) or read-only global
+        auto ld16 = [&](const uint4* src, int j) -> uint4 { return kPrefetch ? src[LPV * j] : __ldg(src + LPV * j); };
 
         // ---- key -----------------------------------------------------------
         {
             float x[EPL];
             if constexpr (KB == 8) {
-                load_bf16<EPL>(k + vsafe * D + part * EPL, x);
-                // FP8 e4m3, round to nearest even, saturating finite.
-                uint32_t w[EPL / 4];
 #pragma unroll
-                for (int j = 0; j < EPL / 4; ++j) {
-                    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * j], x[4 * j + 1]),
-                                                                 __NV_SATFINITE, __NV_E4M3);
-                    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * j + 2], x[4 * j + 3]),
-                                                                 __NV_SATFINITE, __NV_E4M3);
-                    w[j] = (lo & 0xffffu) | (hi << 16);
+                for (int j = 0; j < EPL / 8; ++j) {
+                    const uint4 u = ld16(ksrc, j);
+                    // FP8 e4m3, round to nearest even, saturating finite
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                    uint32_t f[2];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+                            make_float2(bf16_lo(w4[2 * q]), bf16_hi(w4[2 * q])), __NV_SATFINITE, __NV_E4M3);
+                        const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+                            make_float2(bf16_lo(w4[2 * q + 1]), bf16_hi(w4[2 * q + 1])), __NV_SATFINITE, __NV_E4M3);
+                        f[q] = (lo & 0xffffu) | (hi << 16);
+                    }
+                    put_bytes<8>(my_slot + 8 * (part + LPV * j), (static_cast<uint64_t>(f[1]) << 32) | f[0], true);
                 }
-                write_u16_words(my_slot + part * EPL, EPL, w);
             } else {
                 // bf16 pairs with the random signs applied to the raw sign bits
-                const uint4* src = reinterpret_cast<const uint4*>(k + vsafe * D + part * EPL);
                 const uint4* msk = reinterpret_cast<const uint4*>(sign_mask[part]);
 #pragma unroll
                 for (int j = 0; j < EPL / 8; ++j) {
-                    const uint4 u = __ldg(src + j);
+                    const uint4 u = ld16(ksrc, j);
                     const uint4 m = msk[j];
                     const uint32_t w[4] = {u.x ^ m.x, u.y ^ m.y, u.z ^ m.z, u.w ^ m.w};
 #pragma unroll
@@ -154,15 +237,17 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                 float t[kHalf - 1];
 #pragma unroll
                 for (int j = 0; j < kHalf - 1; ++j) t[j] = pos_b[j] * u;
-                uint32_t code[EPL];
 #pragma unroll
-                for (int i = 0; i < EPL; ++i) {
-                    const uint32_t cnt = count_above(fabsf(x[i]), t);
-                    code[i] = x[i] > 0.f ? kHalf + cnt : kHalf - 1 - cnt;
+                for (int j = 0; j < EPL / 8; ++j) {
+                    uint32_t code[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float xe = x[8 * j + e];
+                        const uint32_t cnt = count_above(fabsf(xe), t);
+                        code[e] = xe > 0.f ? kHalf + cnt : kHalf - 1 - cnt;
+                    }
+                    put_bytes<KB>(my_slot + KB * (part + LPV * j), pack8<KB>(code), false);
                 }
-                uint32_t w[(EPL * KB + 31) / 32];
-                pack_codes<EPL, KB>(code, w);
-                write_u16_words(my_slot + part * (EPL * KB / 8), EPL * KB / 8, w);
                 if (part == 0)
                     *reinterpret_cast<uint16_t*>(my_slot + S::kKeyIdxBytes) = half_bits(n);
             }
@@ -171,7 +256,16 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
         // ---- value ---------------------------------------------------------
         {
             float x[EPL];
-            load_bf16<EPL>(v + vsafe * D + part * EPL, x);
+#pragma unroll
+            for (int j = 0; j < EPL / 8; ++j) {
+                const uint4 u = ld16(vsrc, j);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    x[8 * j + 2 * q] = bf16_lo(w[q]);
+                    x[8 * j + 2 * q + 1] = bf16_hi(w[q]);
+                }
+            }
             float mn = x[0], mx = x[0];
 #pragma unroll
             for (int i = 1; i < EPL; ++i) {
@@ -192,8 +286,8 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                 for (int i = 0; i < EPL; ++i) {
                     const float qv = quotient_rn(__fsub_rn(x[i], z), s, y);
                     // clamp, then round half to even by the 1.5 * 2^23 addition
-                    const float c = fminf(fmaxf(qv, 0.f), static_cast<float>(kTopV));
-                    code[i] = __float_as_uint(__fadd_rn(c, 12582912.f)) & static_cast<uint32_t>(kTopV);
+                    const float cl = fminf(fmaxf(qv, 0.f), static_cast<float>(kTopV));
+                    code[i] = __float_as_uint(__fadd_rn(cl, 12582912.f)) & static_cast<uint32_t>(kTopV);
                 }
             } else {
 #pragma unroll
@@ -203,9 +297,9 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                     code[i] = (s == 0.f) ? 0u : static_cast<uint32_t>(r);
                 }
             }
-            uint32_t w[(EPL * VB + 31) / 32];
-            pack_codes<EPL, VB>(code, w);
-            write_u16_words(my_slot + S::kKeyBytes + part * (EPL * VB / 8), EPL * VB / 8, w);
+#pragma unroll
+            for (int j = 0; j < EPL / 8; ++j)
+                put_bytes<VB>(my_slot + S::kKeyBytes + VB * (part + LPV * j), pack8<VB>(code + 8 * j), false);
             if (part == 0) {
                 uint16_t* sz = reinterpret_cast<uint16_t*>(my_slot + S::kKeyBytes + S::kValCodeBytes);
                 sz[0] = sb;
@@ -241,6 +335,13 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
         }
         __syncwarp();
     }
+    if (timed_out) {
+        if (lane == 0) {
+            set_flag(c.flags, kFlagWait);
+            // the other slot may still be filling: wait for it (bounded) before exiting
+            if (base + step < num_vecs) mbar_wait(full_sh + 8u * ((it & 1) ^ 1), static_cast<uint32_t>(((it + 1) >> 1) & 1));
+        }
+    }
 }
 
 template <int D, int KB, int VB>
@@ -252,7 +353,11 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const uint16_t* k, 
     const int64_t want = (warps + kStoreWarps - 1) / kStoreWarps;
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     const int grid = static_cast<int>(want < cap ? want : cap);
-    store_kernel<D, KB, VB><<<grid, kStoreWarps * 32, 0, stream>>>(p, c, k, v, num_tokens, slot_mapping);
+    const int ring_bytes = KB != 8 ? kStoreWarps * 4 * VPW * D * 2 : 0;
+    auto kern = store_kernel<D, KB, VB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ring_bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kStoreWarps * 32, ring_bytes, stream>>>(p, c, k, v, num_tokens, slot_mapping);
     return cudaGetLastError();
 }
 
