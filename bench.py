@@ -97,6 +97,14 @@ def reduce_scalar(x: float, op: str, device=None) -> float:
     return float(t.item())
 
 
+def weak_scaling_value(units: float, seconds: float, device=None) -> float:
+    """Whole-job throughput: the units all ranks processed / the slowest
+    rank's time (max over ranks), as the launch contract defines it."""
+    total = reduce_scalar(units, "sum", device)
+    slowest = reduce_scalar(seconds, "max", device)
+    return total / slowest
+
+
 # ---------------------------------------------------------------------------
 # accounting
 # ---------------------------------------------------------------------------
@@ -312,11 +320,9 @@ def run_ours(args):
 
     packed, algo = decode_bytes(wl, slot_al)
     n_calls = args.steps * len(layers)
-    dec_ms_max = reduce_scalar(dec_ms, "max", dev)
-    store_ms_max = reduce_scalar(store_ms, "max", dev)
     total_ms_max = reduce_scalar(total_ms, "max", dev)
-    value = world * packed * n_calls / (dec_ms_max * 1e-3) / 1e9
-    store_mtok = world * store_n * n_calls / (store_ms_max * 1e-3) / 1e6
+    value = weak_scaling_value(packed * n_calls, dec_ms * 1e-3, dev) / 1e9
+    store_mtok = weak_scaling_value(store_n * n_calls, store_ms * 1e-3, dev) / 1e6
     peak, peak_kind = measured_peaks()
     dec_avg_s = dec_ms / n_calls * 1e-3
     achieved = algo / dec_avg_s / 1e9
