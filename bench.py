@@ -331,6 +331,7 @@ def run_ours(args):
     # ---- end to end through host buffers ---------------------------------------
     e2e = run_e2e(args, tq, wl, cfg, caches, k_new, v_new, slots_new, q, table, lens, max_len, ws, outs, stream,
                   packed, dev)
+    dq = measure_dequant(tq, wl, cfg, caches[0], table, max_len, dev, stream, peak)
 
     clk = clocks.summary()
     result = {
@@ -357,6 +358,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": algo, "avg_launch_us": round(dec_avg_s * 1e6, 2)},
         "e2e": e2e,
         "gpu_launches": n_calls * 3,
+        "dequant": dq,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -378,6 +380,35 @@ def shrink(wl, args):
     elif args.layers:
         wl.description += f" [reduced: {len(wl.layers)} layer(s)]"
     return wl
+
+
+def measure_dequant(tq, wl, cfg, cache, table, max_len, dev, stream, peak, reps=10):
+    """tq_dequant of the workload's decode sequences (continuation prefill),
+    outside the timed step: packed bytes read + bf16 K and V written, per
+    call, over the median CUDA-event time of `reps` calls."""
+    import torch
+
+    lens = wl.seq_lens.astype(np.int64)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(dev)
+    n = int(lens.sum())
+    h, d = wl.num_kv_heads, wl.head_dim
+    k_out = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
+    v_out = torch.empty_like(k_out)
+    for _ in range(3):
+        tq.tq_dequant(cfg, cache, table, cu, max_len, k_out, v_out, stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        tq.tq_dequant(cfg, cache, table, cu, max_len, k_out, v_out, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+    bytes_ = n * h * (cfg.slot_size_aligned + 4 * d)
+    del k_out, v_out
+    return {"value": round(bytes_ / us / 1e3, 1), "unit": "GB/s", "frac": round(bytes_ / us / 1e3 / peak, 4),
+            "us_per_call": round(us, 2), "tokens": n,
+            "bytes_per_call": bytes_, "note": "packed slots read + bf16 K and V written; not part of the timed step"}
 
 
 def run_e2e(args, tq, wl, cfg, caches, k_new, v_new, slots_new, q, table, lens, max_len, ws, outs, stream,

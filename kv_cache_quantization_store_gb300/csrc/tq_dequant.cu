@@ -3,11 +3,15 @@
 // [TQC] TurboQuantConfig.mse_bits docstring: the centroids also serve the
 // continuation-prefill dequant.  Keys: k_hat = vec_norm * Pi^T c~, with c~
 // divided by ||c~|| under norm correction ([TQC] docstring, norm_correction);
-// Pi^T = diag(s) H / sqrt(d), so the FWHT runs first and the signs after.
+// Pi^T = diag(s) H / sqrt(d), so the FWHT runs first and the signs after
+// (a sign flip commutes with the rounding to bf16, so it is applied to the
+// packed bf16 bits).
 // FP8 keys decode their e4m3 bytes.  Values: scale * code + zero.
 //
 // Same lane decomposition as the store: a vector is LPV lane parts of
-// EPL = min(d, 32) elements; each lane writes its part as 16-byte stores.
+// EPL = min(d, 32) elements, part p owning the 8-element groups
+// 8 (p + LPV j) + e, so that a quarter-warp writes 128 contiguous bytes of
+// bf16 and reads whole bytes of codes per group.
 #include "tq_device.cuh"
 
 namespace tq {
@@ -15,20 +19,24 @@ namespace {
 
 constexpr int kDqWarps = 8;
 
-template <int N>
-__device__ __forceinline__ void store_bf16(uint16_t* dst, const float (&x)[N]) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
+// Reads NB bytes (3, 4 or 8) at a 2-byte aligned global address + byte offset
+// `off` (even for NB = 4 and 8) as the low-order bytes of a 64-bit word.
+template <int NB>
+__device__ __forceinline__ uint64_t get_bytes(const uint8_t* p) {
+    if constexpr (NB == 3) {
+        return static_cast<uint64_t>(p[0]) | (static_cast<uint64_t>(p[1]) << 8) | (static_cast<uint64_t>(p[2]) << 16);
+    } else {
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(p);
+        uint64_t w = 0;
 #pragma unroll
-    for (int j = 0; j < N / 8; ++j) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(x[8 * j + 2 * e]));
-            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(x[8 * j + 2 * e + 1]));
-            w[e] = lo | (hi << 16);
-        }
-        d[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < NB / 2; ++i) w |= static_cast<uint64_t>(h[i]) << (16 * i);
+        return w;
     }
+}
+
+__device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
 template <int D, int KB, int VB>
@@ -40,6 +48,10 @@ dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict
     using LS = LaneSplit<D>;
     constexpr int EPL = LS::kEPL, LPV = LS::kLPV, VPW = LS::kVPW;
     constexpr int SA = S::kAligned;
+    // centroid table and, per lane part, XOR masks that apply the random
+    // signs to the packed bf16 pairs of the output (word w of group j at 4 j + w)
+    __shared__ float cent[16];
+    __shared__ __align__(16) uint32_t sign_mask[LPV][EPL / 2];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int part = lane % LPV;
@@ -54,11 +66,16 @@ dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict
         n = n < 0 ? 0 : cap;
     }
     const int64_t num_vecs = static_cast<int64_t>(n) * H;
-
-    uint32_t signs = 0;
     if constexpr (KB != 8) {
-        const int first = part * EPL;
-        signs = p.sign_mask[first / 32] >> (first % 32);
+        if (threadIdx.x < 16) cent[threadIdx.x] = p.centroids[threadIdx.x < p.n_centroids ? threadIdx.x : 0];
+        for (int i = threadIdx.x; i < LPV * EPL / 2; i += kDqWarps * 32) {
+            const int pp = i / (EPL / 2), jw = i % (EPL / 2);
+            const int e = 8 * (pp + LPV * (jw / 4)) + 2 * (jw % 4);
+            const uint32_t b0 = (p.sign_mask[e / 32] >> (e % 32)) & 1u;
+            const uint32_t b1 = (p.sign_mask[(e + 1) / 32] >> ((e + 1) % 32)) & 1u;
+            sign_mask[pp][jw] = (b0 << 15) | (b1 << 31);
+        }
+        __syncthreads();
     }
     const float inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(D));
 
@@ -74,49 +91,69 @@ dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict
         if (valid && !ok && part == 0) set_flag(c.flags, kFlagBlock);
         const uint8_t* slot = c.data + static_cast<int64_t>(ok ? blk : 0) * c.block_stride +
                               (static_cast<int64_t>(pos % c.block_size) * H + h) * SA;
-        const int64_t out_off = ((row0 + pos) * H + h) * D + part * EPL;
+        uint4* kdst = reinterpret_cast<uint4*>(k_out + ((row0 + pos) * H + h) * D) + part;
+        uint4* vdst = reinterpret_cast<uint4*>(v_out + ((row0 + pos) * H + h) * D) + part;
 
         // ---- key -----------------------------------------------------------
-        float x[EPL];
         if constexpr (KB == 8) {
-            uint32_t w[EPL / 4];
-            read_u16_words(slot + part * EPL, EPL, w);
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) x[i] = e4m3_to_float((w[i / 4] >> (8 * (i % 4))) & 0xffu);
+            for (int j = 0; j < EPL / 8; ++j) {
+                const uint64_t b = get_bytes<8>(slot + 8 * (part + LPV * j));
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    w[q] = bf16_pair(e4m3_to_float(static_cast<uint32_t>(b >> (16 * q)) & 0xffu),
+                                     e4m3_to_float(static_cast<uint32_t>(b >> (16 * q + 8)) & 0xffu));
+                if (ok) kdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         } else {
-            constexpr int NW = (EPL * KB + 31) / 32;
-            uint32_t w[NW];
-            read_u16_words(slot + part * (EPL * KB / 8), EPL * KB / 8, w);
+            float x[EPL];
             float nsq = 0.f;
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                x[i] = p.centroids[unpack_code<KB, NW>(w, i)];
-                nsq = fmaf(x[i], x[i], nsq);
+            for (int j = 0; j < EPL / 8; ++j) {
+                const uint64_t b = get_bytes<KB>(slot + KB * (part + LPV * j));
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    x[8 * j + e] = cent[static_cast<uint32_t>(b >> (KB * e)) & ((1u << KB) - 1u)];
+                    nsq = fmaf(x[8 * j + e], x[8 * j + e], nsq);
+                }
             }
             nsq = sum_lanes<LPV>(nsq);
             const float vec_norm = half_from_bits(*reinterpret_cast<const uint16_t*>(slot + S::kKeyIdxBytes));
             float f = vec_norm * inv_sqrt_d;
             if (p.nc) f = f / sqrtf(nsq);
             fwht_local<EPL>(x);
-            fwht_lanes<EPL, LPV>(x, part);
+            fwht_lanes_fma<EPL, LPV>(x, part);
+            const uint4* msk = reinterpret_cast<const uint4*>(sign_mask[part]);
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) x[i] = ((signs >> i) & 1u) ? -x[i] * f : x[i] * f;
+            for (int j = 0; j < EPL / 8; ++j) {
+                const uint4 m = msk[j];
+                const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) w[q] = bf16_pair(x[8 * j + 2 * q] * f, x[8 * j + 2 * q + 1] * f) ^ mw[q];
+                if (ok) kdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
-        if (ok) store_bf16<EPL>(k_out + out_off, x);
 
         // ---- value ---------------------------------------------------------
         {
-            constexpr int NW = (EPL * VB + 31) / 32;
-            uint32_t w[NW];
-            read_u16_words(slot + S::kKeyBytes + part * (EPL * VB / 8), EPL * VB / 8, w);
             const uint16_t* sz = reinterpret_cast<const uint16_t*>(slot + S::kKeyBytes + S::kValCodeBytes);
             const float sc = half_from_bits(sz[0]);
             const float z = half_from_bits(sz[1]);
 #pragma unroll
-            for (int i = 0; i < EPL; ++i)
-                x[i] = fmaf(sc, static_cast<float>(unpack_code<VB, NW>(w, i)), z);
+            for (int j = 0; j < EPL / 8; ++j) {
+                const uint64_t b = get_bytes<VB>(slot + S::kKeyBytes + VB * (part + LPV * j));
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float c0 = static_cast<float>(static_cast<uint32_t>(b >> (VB * 2 * q)) & ((1u << VB) - 1u));
+                    const float c1 = static_cast<float>(static_cast<uint32_t>(b >> (VB * (2 * q + 1))) & ((1u << VB) - 1u));
+                    w[q] = bf16_pair(fmaf(sc, c0, z), fmaf(sc, c1, z));
+                }
+                if (ok) vdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
-        if (ok) store_bf16<EPL>(v_out + out_off, x);
     }
 }
 

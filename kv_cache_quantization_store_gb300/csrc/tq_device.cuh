@@ -37,25 +37,6 @@ struct LaneSplit {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Loads N bf16 values (N a multiple of 8, 16-byte aligned) as fp32.
-template <int N>
-__device__ __forceinline__ void load_bf16(const uint16_t* __restrict__ src, float (&x)[N]) {
-    static_assert(N % 8 == 0, "bf16 loads come in 16-byte units");
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int j = 0; j < N / 8; ++j) {
-        uint4 u = __ldg(s + j);
-        x[8 * j + 0] = bf16_lo(u.x);
-        x[8 * j + 1] = bf16_hi(u.x);
-        x[8 * j + 2] = bf16_lo(u.y);
-        x[8 * j + 3] = bf16_hi(u.y);
-        x[8 * j + 4] = bf16_lo(u.z);
-        x[8 * j + 5] = bf16_hi(u.z);
-        x[8 * j + 6] = bf16_lo(u.w);
-        x[8 * j + 7] = bf16_hi(u.w);
-    }
-}
-
 // In-register Walsh-Hadamard butterflies over the low log2(N) index bits
 // (natural Sylvester order: stage s pairs i and i + s).
 template <int N>
@@ -73,18 +54,15 @@ __device__ __forceinline__ void fwht_local(float (&x)[N]) {
     }
 }
 
-// Butterflies across the LPV lanes of one vector (index bits above the
-// lane-local ones); `part` is this lane's position within the vector.
+// Butterflies across the LPV lanes of one vector as fma(+-1, x, partner):
+// the same single rounding as the add or the subtract it stands for.
 template <int N, int LPV>
-__device__ __forceinline__ void fwht_lanes(float (&x)[N], int part) {
+__device__ __forceinline__ void fwht_lanes_fma(float (&x)[N], int part) {
 #pragma unroll
     for (int m = 1; m < LPV; m <<= 1) {
-        const bool upper = (part & m) != 0;
+        const float sg = (part & m) ? -1.f : 1.f;
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            const float o = __shfl_xor_sync(kFull, x[i], m);
-            x[i] = upper ? (o - x[i]) : (x[i] + o);
-        }
+        for (int i = 0; i < N; ++i) x[i] = fmaf(sg, x[i], __shfl_xor_sync(kFull, x[i], m));
     }
 }
 
@@ -107,51 +85,6 @@ __device__ __forceinline__ float max_lanes(float v) {
 #pragma unroll
     for (int m = 1; m < LPV; m <<= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
     return v;
-}
-
-// Packs N codes of B bits into an LSB-first bitstream held in 32-bit words.
-template <int N, int B>
-__device__ __forceinline__ void pack_codes(const uint32_t (&code)[N], uint32_t (&w)[(N * B + 31) / 32]) {
-#pragma unroll
-    for (int j = 0; j < (N * B + 31) / 32; ++j) w[j] = 0u;
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const int bit = i * B;
-        w[bit / 32] |= code[i] << (bit % 32);
-        if (bit % 32 + B > 32) w[bit / 32 + 1] |= code[i] >> (32 - bit % 32);
-    }
-}
-
-// Extracts code i (B bits) of an LSB-first bitstream given as 32-bit words.
-template <int B, int NW>
-__device__ __forceinline__ uint32_t unpack_code(const uint32_t (&w)[NW], int i) {
-    const int bit = i * B;
-    uint32_t v = w[bit / 32] >> (bit % 32);
-    if (bit % 32 + B > 32) v |= w[bit / 32 + 1] << (32 - bit % 32);
-    return v & ((1u << B) - 1u);
-}
-
-// Reads `nbytes` (even) bytes at a 2-byte aligned shared/global address into
-// little-endian 32-bit words.
-template <int NW>
-__device__ __forceinline__ void read_u16_words(const uint8_t* p, int nbytes, uint32_t (&w)[NW]) {
-    const uint16_t* h = reinterpret_cast<const uint16_t*>(p);
-#pragma unroll
-    for (int j = 0; j < NW; ++j) {
-        const uint32_t lo = (4 * j < nbytes) ? h[2 * j] : 0u;
-        const uint32_t hi = (4 * j + 2 < nbytes) ? h[2 * j + 1] : 0u;
-        w[j] = lo | (hi << 16);
-    }
-}
-
-template <int NW>
-__device__ __forceinline__ void write_u16_words(uint8_t* p, int nbytes, const uint32_t (&w)[NW]) {
-    uint16_t* h = reinterpret_cast<uint16_t*>(p);
-#pragma unroll
-    for (int j = 0; j < NW; ++j) {
-        if (4 * j < nbytes) h[2 * j] = static_cast<uint16_t>(w[j] & 0xffffu);
-        if (4 * j + 2 < nbytes) h[2 * j + 1] = static_cast<uint16_t>(w[j] >> 16);
-    }
 }
 
 __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {

@@ -20,18 +20,6 @@ namespace {
 
 constexpr int kStoreWarps = 8;
 
-// Butterflies across the LPV lanes of one vector as fma(+-1, x, partner):
-// the same single rounding as the add or the subtract it stands for.
-template <int N, int LPV>
-__device__ __forceinline__ void fwht_lanes_fma(float (&x)[N], int part) {
-#pragma unroll
-    for (int m = 1; m < LPV; m <<= 1) {
-        const float sg = (part & m) ? -1.f : 1.f;
-#pragma unroll
-        for (int i = 0; i < N; ++i) x[i] = fmaf(sg, x[i], __shfl_xor_sync(kFull, x[i], m));
-    }
-}
-
 // Number of the positive decision thresholds t[0] < t[1] < ... below a >= 0
 // (strictly), by binary search over the 3 (3-bit) or 7 (4-bit) thresholds.
 template <int NT>
