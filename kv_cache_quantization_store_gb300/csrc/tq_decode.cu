@@ -306,26 +306,95 @@ decode_kernel(const LayerParams p, const CacheGeom c, const DecodeArgs a) {
     }
 }
 
-// Log-sum-exp merge of the split partials: one CTA per (query head, sequence),
-// one thread per output dimension.
-__global__ void combine_kernel(const float* __restrict__ partials, float* __restrict__ out, int Hq, int D,
-                               int num_splits) {
+// Log-sum-exp merge of the split partials: one CTA per (query head,
+// sequence) with nw warps (nw grows with the split count).  Warp w merges
+// splits w, w + nw, ... on its own: its lanes first fold the splits' (m, l)
+// with a running maximum, then sum the weighted o over those splits (two
+// dims per lane and load, the splits' loads independent of one another).
+// With several warps their (m, l, o) meet in shared memory.
+constexpr int kCombineMaxWarps = 8;
+
+// 2^(m - M), 0 for a split without tokens (m = -inf)
+__device__ __forceinline__ float lse_weight(float m, float M) { return m == -INFINITY ? 0.f : exp2f(m - M); }
+
+__global__ void __launch_bounds__(32 * kCombineMaxWarps)
+combine_kernel(const float* __restrict__ partials, float* __restrict__ out, int Hq, int D, int num_splits) {
+    __shared__ float wm[kCombineMaxWarps], wl[kCombineMaxWarps];
+    __shared__ float wacc[kCombineMaxWarps][256];
     const int hq = blockIdx.x, s = blockIdx.y;
-    const float* base = partials + (static_cast<int64_t>(s) * Hq + hq) * num_splits * (D + 2);
-    float M = -INFINITY;
-    for (int sp = 0; sp < num_splits; ++sp) M = fmaxf(M, base[sp * (D + 2)]);
-    for (int i = threadIdx.x; i < D; i += blockDim.x) {
-        float lsum = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
-            for (int sp = 0; sp < num_splits; ++sp) {
-                const float m = base[sp * (D + 2)];
-                if (m == -INFINITY) continue;
-                const float w = exp2f(m - M);
-                lsum = fmaf(base[sp * (D + 2) + 1], w, lsum);
-                acc = fmaf(base[sp * (D + 2) + 2 + i], w, acc);
+    const int row = D + 2;
+    const float* base = partials + (static_cast<int64_t>(s) * Hq + hq) * num_splits * row;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    // (m, l) of this warp's splits, folded per lane, then across the lanes
+    float M = -INFINITY, L = 0.f;
+    for (int sp = warp + nw * lane; sp < num_splits; sp += 32 * nw) {
+        const float m = base[static_cast<int64_t>(sp) * row], l = base[static_cast<int64_t>(sp) * row + 1];
+        const float nm = fmaxf(M, m);
+        L = L * lse_weight(M, nm) + l * lse_weight(m, nm);
+        M = nm;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, M, o), ol = __shfl_xor_sync(0xffffffffu, L, o);
+        const float nm = fmaxf(M, om);
+        L = L * lse_weight(M, nm) + ol * lse_weight(om, nm);
+        M = nm;
+    }
+    // weighted o of this warp's splits: lane covers float2 columns lane + 32 j
+    float2 acc[4] = {};
+    const int ncol = D / 2;
+    if (M != -INFINITY) {
+#pragma unroll 4
+        for (int sp = warp; sp < num_splits; sp += nw) {
+            const float* ps = base + static_cast<int64_t>(sp) * row;
+            const float w = lse_weight(ps[0], M);
+            const float2* o2 = reinterpret_cast<const float2*>(ps + 2);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = lane + 32 * j;
+                if (col < ncol) {
+                    const float2 o = o2[col];
+                    acc[j].x = fmaf(o.x, w, acc[j].x);
+                    acc[j].y = fmaf(o.y, w, acc[j].y);
+                }
             }
         }
-        out[(static_cast<int64_t>(s) * Hq + hq) * D + i] = lsum > 0.f ? acc / lsum : 0.f;
+    }
+    float* dst = out + (static_cast<int64_t>(s) * Hq + hq) * D;
+    if (nw == 1) {
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = lane + 32 * j;
+            if (col < ncol) {  // out is only 4-byte aligned
+                dst[2 * col] = acc[j].x * inv;
+                dst[2 * col + 1] = acc[j].y * inv;
+            }
+        }
+        return;
+    }
+    if (lane == 0) {
+        wm[warp] = M;
+        wl[warp] = L;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int col = lane + 32 * j;
+        if (col < ncol) {
+            wacc[warp][2 * col] = acc[j].x;
+            wacc[warp][2 * col + 1] = acc[j].y;
+        }
+    }
+    __syncthreads();
+    float Mt = -INFINITY;
+    for (int w = 0; w < nw; ++w) Mt = fmaxf(Mt, wm[w]);
+    float Lt = 0.f;
+    for (int w = 0; w < nw; ++w) Lt = fmaf(wl[w], lse_weight(wm[w], Mt), Lt);
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        float a = 0.f;
+        for (int w = 0; w < nw; ++w) a = fmaf(wacc[w][i], lse_weight(wm[w], Mt), a);
+        dst[i] = a * inv;
     }
 }
 
@@ -361,7 +430,11 @@ cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const Decode
 cudaError_t launch_combine(const float* partials, float* out, int num_seqs, int num_q_heads, int d,
                            int num_splits, cudaStream_t stream) {
     dim3 cgrid(static_cast<unsigned>(num_q_heads), static_cast<unsigned>(num_seqs));
-    combine_kernel<<<cgrid, d < 128 ? 128 : d, 0, stream>>>(partials, out, num_q_heads, d, num_splits);
+    if (d > 256 || d % 2 != 0) return cudaErrorInvalidValue;
+    // about 8 splits per warp, at most kCombineMaxWarps warps
+    int nw = (num_splits + 7) / 8;
+    nw = nw < 1 ? 1 : (nw > kCombineMaxWarps ? kCombineMaxWarps : nw);
+    combine_kernel<<<cgrid, 32 * nw, 0, stream>>>(partials, out, num_q_heads, d, num_splits);
     return cudaGetLastError();
 }
 

@@ -43,6 +43,7 @@
 // partial it reads, so the workspace needs no clearing between calls.
 #pragma once
 
+#include <atomic>
 #include <cmath>
 #include <type_traits>
 
@@ -942,15 +943,44 @@ struct Kernel {
     using G = Geo<D, KB, VB, H, P::WPH, P::NS, PACKQ>;
     static constexpr auto fn = decode_kernel<D, KB, VB, NC, H, P::WPH, P::NS, P::MINB, PACKQ>;
 
+    // Per device (function attributes belong to a device's context): the
+    // largest dynamic shared memory granted so far, and the resident CTAs per
+    // SM per query-head count, so that repeated calls skip the driver queries.
+    static constexpr int kDevs = 16;
+    static inline std::atomic<int> granted[kDevs] = {};
+    static inline std::atomic<int> ctas_cache[kDevs][65] = {};
+    static int device() {
+        int dev = -1;
+        return cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kDevs ? dev : -1;
+    }
     static cudaError_t prepare(int hq, int* smem) {
         *smem = G::smem_bytes(hq);
-        return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, *smem);
+        const int dev = device();
+        if (dev >= 0 && *smem <= granted[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, *smem);
+        if (e == cudaSuccess && dev >= 0) {
+            int cur = granted[dev].load(std::memory_order_relaxed);
+            while (cur < *smem && !granted[dev].compare_exchange_weak(cur, *smem)) {
+            }
+        }
+        return e;
     }
     static cudaError_t occupancy(int hq, int* ctas) {
+        const int dev = device();
+        const bool cacheable = dev >= 0 && hq >= 0 && hq <= 64;
+        if (cacheable) {
+            const int v = ctas_cache[dev][hq].load(std::memory_order_relaxed);
+            if (v > 0) {
+                *ctas = v;
+                return cudaSuccess;
+            }
+        }
         int smem = 0;
-        const cudaError_t e = prepare(hq, &smem);
+        cudaError_t e = prepare(hq, &smem);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, fn, G::NT, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, fn, G::NT, smem);
+        if (e == cudaSuccess && cacheable) ctas_cache[dev][hq].store(*ctas, std::memory_order_relaxed);
+        return e;
     }
     static cudaError_t launch(const LayerParams& p, const CacheGeom& c, const Args& a, int num_seqs,
                               cudaStream_t stream) {

@@ -98,11 +98,43 @@ constexpr Preset kPresets[] = {
 
 // Recomputes every derived field of a caller-supplied config and builds the
 // kernel parameters; rejects configs that were edited inconsistently.
+// The argument checks and slot sizes of a configuration ([TQC]
+// key_packed_size / value_packed_size / slot_size_aligned); no codebook.
+tq_status config_sizes(int32_t head_dim, int32_t key_quant_bits, int32_t value_quant_bits, int32_t norm_correction,
+                       uint64_t seed, tq_config* out) {
+    if (head_dim <= 0) return fail(TQ_ERR_INVALID_ARG, "head_dim must be positive (got %d)", head_dim);
+    if (!tq::supported_head_dim(head_dim))
+        return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: the Walsh-Hadamard rotation needs a power of two in [16, 256]",
+                    head_dim);
+    if (key_quant_bits != 3 && key_quant_bits != 4 && key_quant_bits != 8)
+        return fail(TQ_ERR_INVALID_ARG, "key_quant_bits must be 3, 4 (Lloyd-Max) or 8 (FP8), got %d",
+                    key_quant_bits);
+    if (value_quant_bits != 3 && value_quant_bits != 4)
+        return fail(TQ_ERR_INVALID_ARG, "value_quant_bits must be 3 or 4, got %d", value_quant_bits);
+    tq_config& c = *out;
+    std::memset(&c, 0, sizeof c);
+    c.head_dim = head_dim;
+    c.key_quant_bits = key_quant_bits;
+    c.value_quant_bits = value_quant_bits;
+    c.norm_correction = norm_correction ? 1 : 0;
+    c.seed = seed;
+    c.key_fp8 = key_quant_bits == 8;
+    c.mse_bits = c.key_fp8 ? value_quant_bits : key_quant_bits;
+    c.key_mse_bits = c.key_fp8 ? 0 : key_quant_bits;
+    c.n_centroids = 1 << c.mse_bits;
+    c.key_packed_size = c.key_fp8 ? head_dim : ceil_div(head_dim * c.key_mse_bits, 8) + 2;
+    c.value_packed_size = ceil_div(head_dim * value_quant_bits, 8) + 4;
+    c.slot_size = c.key_packed_size + c.value_packed_size;
+    c.slot_size_aligned = c.slot_size + (c.slot_size & 1);
+
+    return TQ_OK;
+}
+
 tq_status layer_params(const tq_config* cfg, int layer_idx, tq::LayerParams* lp) {
     if (cfg == nullptr) return fail(TQ_ERR_INVALID_ARG, "config is NULL");
-    tq_config ref;
-    const tq_status st = tq_config_init(cfg->head_dim, cfg->key_quant_bits, cfg->value_quant_bits,
-                                        cfg->norm_correction, cfg->seed, &ref);
+    tq_config ref;  // sizes only: the codebook is the config's own
+    const tq_status st = config_sizes(cfg->head_dim, cfg->key_quant_bits, cfg->value_quant_bits,
+                                      cfg->norm_correction, cfg->seed, &ref);
     if (st != TQ_OK) return st;
     if (ref.slot_size_aligned != cfg->slot_size_aligned || ref.key_packed_size != cfg->key_packed_size ||
         ref.value_packed_size != cfg->value_packed_size || ref.n_centroids != cfg->n_centroids)
@@ -187,30 +219,9 @@ const char* tq_last_error(void) { return g_last_error; }
 tq_status tq_config_init(int32_t head_dim, int32_t key_quant_bits, int32_t value_quant_bits,
                          int32_t norm_correction, uint64_t seed, tq_config* out) {
     if (out == nullptr) return fail(TQ_ERR_INVALID_ARG, "output config is NULL");
-    if (head_dim <= 0) return fail(TQ_ERR_INVALID_ARG, "head_dim must be positive (got %d)", head_dim);
-    if (!tq::supported_head_dim(head_dim))
-        return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: the Walsh-Hadamard rotation needs a power of two in [16, 256]",
-                    head_dim);
-    if (key_quant_bits != 3 && key_quant_bits != 4 && key_quant_bits != 8)
-        return fail(TQ_ERR_INVALID_ARG, "key_quant_bits must be 3, 4 (Lloyd-Max) or 8 (FP8), got %d",
-                    key_quant_bits);
-    if (value_quant_bits != 3 && value_quant_bits != 4)
-        return fail(TQ_ERR_INVALID_ARG, "value_quant_bits must be 3 or 4, got %d", value_quant_bits);
     tq_config c;
-    std::memset(&c, 0, sizeof c);
-    c.head_dim = head_dim;
-    c.key_quant_bits = key_quant_bits;
-    c.value_quant_bits = value_quant_bits;
-    c.norm_correction = norm_correction ? 1 : 0;
-    c.seed = seed;
-    c.key_fp8 = key_quant_bits == 8;
-    c.mse_bits = c.key_fp8 ? value_quant_bits : key_quant_bits;
-    c.key_mse_bits = c.key_fp8 ? 0 : key_quant_bits;
-    c.n_centroids = 1 << c.mse_bits;
-    c.key_packed_size = c.key_fp8 ? head_dim : ceil_div(head_dim * c.key_mse_bits, 8) + 2;
-    c.value_packed_size = ceil_div(head_dim * value_quant_bits, 8) + 4;
-    c.slot_size = c.key_packed_size + c.value_packed_size;
-    c.slot_size_aligned = c.slot_size + (c.slot_size & 1);
+    const tq_status sz = config_sizes(head_dim, key_quant_bits, value_quant_bits, norm_correction, seed, &c);
+    if (sz != TQ_OK) return sz;
 
     std::vector<double> pos;
     const int iters = lloyd_max_positive(c.n_centroids, pos);

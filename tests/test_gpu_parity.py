@@ -98,6 +98,23 @@ def test_decode_any_split_count(cuda_device, wl):
         assert_rows_close(gpu_decode(wl, cfg, cache, q, cuda_device, num_splits=splits), want)
 
 
+@pytest.mark.parametrize("splits", [300, 520])
+def test_decode_more_splits_than_combine_lanes(cuda_device, splits):
+    """More splits than the combine's 8 warps x 32 lanes: each lane folds
+    several splits' (m, l); the short sequences leave most splits empty."""
+    wl = W.custom(64, 4, 4, True, 2, 8, 16, [8300, 40, 1], 2008)
+    layer_idx = wl.layers[-1]
+    k, v = wl.kv()
+    layer = oracle_layer(wl, layer_idx)
+    ocache, _ = oracle_cache(wl, layer, k, v)
+    cfg = host_cfg(wl)
+    cache = upload_cache(ocache, cfg, layer_idx, cuda_device)
+    q = wl.q()
+    want = O.decode_attention(layer, q, ocache, wl.layout()[0], wl.seq_lens)
+    assert_rows_close(gpu_decode(wl, cfg, cache, q, cuda_device, num_splits=splits), want)
+    assert cache.error_flags() == 0
+
+
 @pytest.mark.parametrize("wl", CASES, ids=IDS)
 def test_dequant_parity(cuda_device, wl):
     layer_idx = wl.layers[-1]
