@@ -20,15 +20,21 @@ Sources (cited by page title and section):
          fixes page-size alignment", section "key source snippet"
          (vllm/platforms/interface.py, _align_hybrid_block_size).
   [ART]  hnwysp.cn TurboQuant article, section "Direction 1: fused Triton
-         kernels" (rotate the query, online softmax block by block).
+         kernels" (rotate the query, online softmax block by block), and
+         section "full_tq zero-allocation mode", item 3 (the write path: an
+         exact bf16 ring of 128 tokens, compressed a whole block at a time).
 
 Pins (tests/test_oracle_pins.py): slot sizes and the compression column of
 the [TQC] preset table, the per-layer seed rule, published SplitMix64 test
 vectors, Sylvester-Hadamard orthogonality and the FWHT, Lloyd-Max fixed-point
 conditions plus Max's (1960) published N(0,1) quantiser tables and the 1-bit
 closed form sqrt(2/pi), exhaustive e4m3 encode against a brute-force nearest
-search, value-quantiser invariants, brute-force decode special cases and
-split invariance of the log-sum-exp merge.
+search, value-quantiser invariants, brute-force decode special cases,
+split invariance of the log-sum-exp merge, and for the ring: token-by-token
+appends equal one plain store of the whole blocks (bytes) with the rest
+verbatim in the ring, chunked appends equal single steps, and the ring
+decode reduces to the packed decode or to closed forms (one token, equal
+keys).
 
 Parity unpinned: byte-for-byte agreement with vLLM's own cache.  The pages do
 not print the random-sign generator, the Hadamard row order or TQ_PRESETS, so
@@ -692,3 +698,94 @@ def merge_partials(parts):
     lsum = sum(p[1] * math.exp(p[0] - m) for p in parts)
     o = sum(p[2] * math.exp(p[0] - m) for p in parts)
     return o / lsum
+
+
+# ---------------------------------------------------------------------------
+# Ring-buffered store  ([ART] hnwysp.cn article, "full_tq zero-allocation
+# mode", item 3 "the write path": new decode tokens first go into an exact
+# bf16 ring of 128 tokens, and only a full ring is compressed, a whole block
+# at a time, so that no single token pays the quantiser on the hot path)
+# ---------------------------------------------------------------------------
+
+#: ring length the article names
+RING_TOKENS = 128
+
+
+def ring_split(seq_len: int, ring_tokens: int) -> tuple[int, int]:
+    """(packed, in ring) token counts of a sequence of seq_len tokens.
+
+    Reading (the article gives the ring's size and flush rule, not its
+    alignment): ring blocks are aligned to multiples of the ring length from
+    position 0, so the whole blocks are packed and the remainder waits in the
+    ring, token p in ring row p mod R.
+    """
+    packed = (seq_len // ring_tokens) * ring_tokens
+    return packed, seq_len - packed
+
+
+def ring_append(layer: Layer, cache: PagedCache, block_table: np.ndarray, ring_k: np.ndarray, ring_v: np.ndarray,
+                seq_lens: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, cu_new: np.ndarray):
+    """Append new tokens to sequences whose newest tokens wait in a ring.
+
+    ring_k, ring_v: [S, R, H, d] exact rows, updated in place; seq_lens[s]:
+    tokens of sequence s before the call (negative: the sequence takes no
+    tokens); its new tokens are rows cu_new[s] .. cu_new[s+1]-1 of k_new,
+    v_new [T, H, d], at positions seq_lens[s], seq_lens[s] + 1, ...  Every
+    ring block that the new tokens complete is quantised into the packed
+    cache at its positions (block_table gives the blocks); the tokens of the
+    block that stays incomplete are written exactly into the ring.  A decode
+    step is one new token per sequence.  Returns {(s, position): near mask
+    [H, d]} for the tokens quantised by this call.
+    """
+    r_len = ring_k.shape[1]
+    near_out = {}
+    for s in range(len(seq_lens)):
+        old = int(seq_lens[s])
+        if old < 0:
+            continue
+        a, b = int(cu_new[s]), int(cu_new[s + 1])
+        total = old + (b - a)
+        old_packed, _ = ring_split(old, r_len)
+        new_packed, _ = ring_split(total, r_len)
+        # exact rows of positions old_packed .. total - 1: the ring's, then the new ones
+        pos = np.arange(old_packed, total)
+        rows_k = np.concatenate([ring_k[s, pos[pos < old] % r_len], k_new[a:b]])
+        rows_v = np.concatenate([ring_v[s, pos[pos < old] % r_len], v_new[a:b]])
+        full = pos < new_packed
+        if full.any():
+            p = pos[full]
+            slots = np.asarray(block_table[s], dtype=np.int64)[p // cache.block_size] * cache.block_size \
+                + p % cache.block_size
+            near = store_kv(layer, rows_k[full], rows_v[full], slots, cache)
+            for i, pp in enumerate(p):
+                near_out[(s, int(pp))] = near[i]
+        tail = ~full
+        ring_k[s, pos[tail] % r_len] = rows_k[tail]
+        ring_v[s, pos[tail] % r_len] = rows_v[tail]
+    return near_out
+
+
+def decode_attention_ring(layer: Layer, q: np.ndarray, cache: PagedCache, block_table: np.ndarray,
+                          seq_lens: np.ndarray, ring_k: np.ndarray, ring_v: np.ndarray,
+                          sm_scale: float | None = None) -> np.ndarray:
+    """Decode over a packed history plus its exact ring (the article's
+    hybrid mode: history from the compressed store, the newest tokens from
+    the exact ring).  Sequence s of seq_lens[s] tokens attends over k_hat,
+    v_hat of its ring_split packed tokens followed by the exact ring rows
+    0 .. n - 1 (positions packed .. seq_len - 1).  Returns fp64 [S, Hq, d]."""
+    cfg = layer.cfg
+    n_seq, hq_n, d = q.shape
+    h_n = cache.num_kv_heads
+    group = hq_n // h_n
+    r_len = ring_k.shape[1]
+    scale = 1.0 / math.sqrt(d) if sm_scale is None or sm_scale <= 0 else sm_scale
+    out = np.zeros((n_seq, hq_n, d))
+    for s in range(n_seq):
+        packed, n_ring = ring_split(max(int(seq_lens[s]), 0), r_len)
+        for h in range(h_n):
+            k_hat, v_hat = dequant_slots(layer, read_slots(cache, block_table[s], packed, h))
+            k_all = np.concatenate([k_hat, ring_k[s, :n_ring, h].astype(np.float64)])
+            v_all = np.concatenate([v_hat, ring_v[s, :n_ring, h].astype(np.float64)])
+            for hq in range(h * group, (h + 1) * group):
+                out[s, hq] = attention_row(q[s, hq], k_all, v_all, scale)
+    return out

@@ -448,3 +448,91 @@ def test_split_merge_is_exact():
         edges = [0, *cuts, 101]
         parts = [O.partial_state(q, kh[a:b], vh[a:b], 0.25) for a, b in zip(edges[:-1], edges[1:])]
         np.testing.assert_allclose(O.merge_partials(parts), full, rtol=1e-12, atol=1e-13)
+
+
+# ---- ring-buffered store ([ART] article, full_tq write path) ---------------------------
+
+def _ring_inputs(rng, lens, h_n, d):
+    k = [O.bf16_round(rng.standard_normal((n, h_n, d)).astype(np.float32)) for n in lens]
+    v = [O.bf16_round(rng.standard_normal((n, h_n, d)).astype(np.float32)) for n in lens]
+    return k, v
+
+
+def _ring_setup(layer, lens, h_n, r_len, block_size=16):
+    nblk = [max(1, -(-n // block_size)) for n in lens]
+    table = np.zeros((len(lens), max(nblk)), dtype=np.int64)
+    perm = np.random.default_rng(11).permutation(sum(nblk))
+    off = 0
+    for s, nb in enumerate(nblk):
+        table[s, :nb] = perm[off:off + nb]
+        off += nb
+    cache = O.new_cache(layer.cfg, sum(nblk), block_size, h_n)
+    d = layer.cfg.head_dim
+    ring_k = np.zeros((len(lens), r_len, h_n, d), dtype=np.float32)
+    return cache, table, ring_k, ring_k.copy()
+
+
+def test_ring_steps_pack_exactly_the_whole_blocks():
+    """Token-by-token appends leave the same packed bytes as one plain store
+    of every whole ring block, and the remainder verbatim in the ring."""
+    cfg = O.Config(head_dim=16, key_quant_bits=3, value_quant_bits=4, norm_correction=True)
+    layer = O.make_layer(cfg, 0)
+    lens, r_len, h_n = [70, 33, 32], 32, 2
+    k, v = _ring_inputs(np.random.default_rng(21), lens, h_n, 16)
+    cache, table, ring_k, ring_v = _ring_setup(layer, lens, h_n, r_len)
+    for step in range(max(lens)):
+        cur = np.array([step if step < n else -1 for n in lens])
+        ks = np.stack([k[s][min(step, n - 1)] for s, n in enumerate(lens)])
+        vs = np.stack([v[s][min(step, n - 1)] for s, n in enumerate(lens)])
+        O.ring_append(layer, cache, table, ring_k, ring_v, cur, ks, vs, np.arange(len(lens) + 1))
+    want = O.new_cache(cfg, cache.num_blocks, cache.block_size, h_n)
+    for s, n in enumerate(lens):
+        packed = (n // r_len) * r_len
+        assert O.ring_split(n, r_len) == (packed, n - packed)
+        pos = np.arange(packed)
+        O.store_kv(layer, k[s][:packed], v[s][:packed], table[s][pos // 16] * 16 + pos % 16, want)
+        np.testing.assert_array_equal(ring_k[s, :n - packed], k[s][packed:])
+        np.testing.assert_array_equal(ring_v[s, :n - packed], v[s][packed:])
+    np.testing.assert_array_equal(cache.data, want.data)
+    assert cache.data.any()
+
+
+def test_ring_chunked_append_equals_steps():
+    """A prefill chunk and a later chunk give the state that single-token
+    steps give (the chunk crosses two ring blocks)."""
+    cfg = O.Config(head_dim=16, key_quant_bits=8, value_quant_bits=3)
+    layer = O.make_layer(cfg, 0)
+    lens, r_len, h_n = [100], 32, 1
+    k, v = _ring_inputs(np.random.default_rng(22), lens, h_n, 16)
+    c1, table, rk1, rv1 = _ring_setup(layer, lens, h_n, r_len)
+    O.ring_append(layer, c1, table, rk1, rv1, np.array([0]), k[0][:45], v[0][:45], np.array([0, 45]))
+    O.ring_append(layer, c1, table, rk1, rv1, np.array([45]), k[0][45:], v[0][45:], np.array([0, 55]))
+    c2, _, rk2, rv2 = _ring_setup(layer, lens, h_n, r_len)
+    for p in range(100):
+        O.ring_append(layer, c2, table, rk2, rv2, np.array([p]), k[0][p:p + 1], v[0][p:p + 1], np.array([0, 1]))
+    np.testing.assert_array_equal(c1.data, c2.data)
+    np.testing.assert_array_equal(rk1[:, :100 % r_len], rk2[:, :100 % r_len])
+    np.testing.assert_array_equal(rv1[:, :100 % r_len], rv2[:, :100 % r_len])
+
+
+def test_ring_decode_reduces_to_packed_decode_and_closed_forms():
+    cfg = O.Config(head_dim=16, key_quant_bits=4, value_quant_bits=4, norm_correction=True)
+    layer = O.make_layer(cfg, 0)
+    lens, r_len, h_n = [64, 1, 20], 32, 1
+    k, v = _ring_inputs(np.random.default_rng(23), lens, h_n, 16)
+    k[2][:] = k[2][:1]  # identical keys in the third sequence's ring
+    cache, table, ring_k, ring_v = _ring_setup(layer, lens, h_n, r_len)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    O.ring_append(layer, cache, table, ring_k, ring_v, np.zeros(3, dtype=np.int64), np.concatenate(k),
+                  np.concatenate(v), cu)
+    q = O.bf16_round(np.random.default_rng(24).standard_normal((3, 2, 16)).astype(np.float32))
+    got = O.decode_attention_ring(layer, q, cache, table, np.array(lens), ring_k, ring_v)
+    # 64 tokens = two whole ring blocks: nothing in the ring, the plain packed decode
+    plain = O.decode_attention(layer, q, cache, table, np.array(lens))
+    np.testing.assert_array_equal(got[0], plain[0])
+    # one token, exact in the ring: the output is that value row
+    np.testing.assert_array_equal(got[1, 0], v[1][0, 0].astype(np.float64))
+    # identical exact keys: the mean of the exact values
+    np.testing.assert_allclose(got[2, 1], v[2][:, 0].astype(np.float64).mean(axis=0), rtol=1e-12, atol=1e-13)
+    # no tokens: zero rows
+    assert not O.decode_attention_ring(layer, q, cache, table, np.array([0, 0, 0]), ring_k, ring_v).any()
