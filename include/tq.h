@@ -227,6 +227,76 @@ TQ_API tq_status tq_dequant(const tq_config* cfg, const tq_cache* cache, const i
                      int32_t max_seq_len, void* k_out_dev, void* v_out_dev, void* stream);
 
 /*
+ * Ring-buffered store ([ART] hnwysp.cn article, "full_tq zero-allocation
+ * mode", item 3 "the write path": new decode tokens first enter an exact
+ * bf16 ring of 128 tokens and only a full ring is compressed, a whole block
+ * at a time).  With a ring of R tokens, a sequence of L tokens keeps the
+ * positions [0, R floor(L/R)) packed in the paged cache and the rest exact,
+ * position p in ring row p mod R of
+ *   ring_k_dev, ring_v_dev: bf16 [num_seqs, R, num_kv_heads, head_dim]
+ * (reading: ring blocks are aligned to multiples of R from position 0; the
+ * caller owns the rings, which need no initialisation).
+ */
+#define TQ_RING_TOKENS 128     /* the ring length the article names */
+#define TQ_RING_MAX_TOKENS 128 /* largest ring the decode accepts */
+
+/* Device workspace bytes of tq_ring_append for num_seqs sequences. */
+TQ_API size_t tq_ring_workspace_size(int32_t num_seqs);
+
+/*
+ * tq_ring_append -- append new tokens to ring-buffered sequences.  Sequence
+ * s holds seq_lens_dev[s] tokens before the call (negative: it takes none)
+ * and its new tokens are rows cu_new_dev[s] .. cu_new_dev[s+1]-1 of
+ *   k_dev, v_dev: bf16 [num_tokens, num_kv_heads, head_dim] (16-byte aligned)
+ * at positions seq_lens[s], seq_lens[s] + 1, ...  Every ring block the new
+ * tokens complete is quantised exactly as tq_store_kv would quantise its
+ * tokens and written to its positions through block_table_dev (int32
+ * [num_seqs, max_blocks_per_seq]); the tokens after the last whole block
+ * are copied into the ring.  A decode step is one token per sequence
+ * (cu_new = 0, 1, ..., num_seqs); a prefill is the prompt with seq_lens 0.
+ *   ring_tokens: R in [1, TQ_RING_MAX_TOKENS]; the same R for every call
+ *   workspace_dev: >= tq_ring_workspace_size(num_seqs) bytes, 16-byte
+ *                  aligned, no initialisation
+ * A sequence whose new length exceeds max_blocks_per_seq * block_size, or
+ * whose cu_new range leaves [0, num_tokens], takes no tokens and sets
+ * TQ_FLAG_SEQ_TOO_LONG; a block_table entry outside the cache sets
+ * TQ_FLAG_BLOCK_OUT_OF_RANGE and that token is not written.  Concurrent
+ * calls sharing one workspace race.
+ */
+TQ_API tq_status tq_ring_append(const tq_config* cfg, const void* k_dev, const void* v_dev, int64_t num_tokens,
+                                const int32_t* cu_new_dev, int32_t num_seqs, const int32_t* seq_lens_dev,
+                                void* ring_k_dev, void* ring_v_dev, int32_t ring_tokens, const tq_cache* cache,
+                                const int32_t* block_table_dev, int32_t max_blocks_per_seq, void* workspace_dev,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * tq_decode_ring_workspace_size -- as tq_decode_workspace_size, for
+ * tq_decode_attention_ring (one more partial state per query head).
+ */
+TQ_API size_t tq_decode_ring_workspace_size(const tq_config* cfg, int32_t num_seqs, int32_t num_q_heads,
+                                            int32_t num_kv_heads, int32_t block_size, int32_t max_seq_len,
+                                            int32_t num_splits);
+
+/*
+ * tq_decode_attention_ring -- tq_decode_attention for ring-buffered
+ * sequences (the article's hybrid mode: history from the compressed store,
+ * the newest tokens from the exact ring).  seq_lens_dev[s] = L counts all
+ * of a sequence's tokens: the packed positions [0, R floor(L/R)) are read
+ * from the cache as tq_decode_attention reads them, and ring rows 0 .. (L
+ * mod R) - 1 exactly (fp32 scores and sums); one softmax covers both.
+ * Arguments as tq_decode_attention, plus the rings of tq_ring_append and R;
+ * workspace >= tq_decode_ring_workspace_size(...).  Up to 8 query heads per
+ * KV head.
+ */
+TQ_API tq_status tq_decode_attention_ring(const tq_config* cfg, const void* q_dev, int32_t num_seqs,
+                                          int32_t num_q_heads, const tq_cache* cache,
+                                          const int32_t* block_table_dev, int32_t max_blocks_per_seq,
+                                          const int32_t* seq_lens_dev, int32_t max_seq_len, float sm_scale,
+                                          int32_t num_splits, const void* ring_k_dev, const void* ring_v_dev,
+                                          int32_t ring_tokens, float* out_dev, void* workspace_dev,
+                                          size_t workspace_bytes, void* stream);
+
+/*
  * tq_hybrid_page -- per-token page geometry of a TQ layer in a hybrid model
  * ([PR] _align_hybrid_block_size snippet).  The TQ page of one token is
  * num_kv_heads * slot_size_aligned bytes (reading of TQFullAttentionSpec with

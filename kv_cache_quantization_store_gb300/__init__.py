@@ -20,7 +20,8 @@ __all__ = [
     "TQError", "TqConfig", "TqCache", "PagedCache", "lib", "library_path",
     "tq_config_init", "tq_config_from_preset", "tq_layer_signs", "tq_store_kv",
     "tq_decode_workspace_size", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_dequant",
-    "tq_status_str", "TQ_NOALLOC_SCRATCH_BYTES",
+    "tq_ring_workspace_size", "tq_ring_append", "tq_decode_ring_workspace_size", "tq_decode_attention_ring",
+    "new_ring", "tq_status_str", "TQ_NOALLOC_SCRATCH_BYTES", "TQ_RING_TOKENS",
     "new_paged_cache", "tq_hybrid_page", "PRESETS",
 ]
 
@@ -32,6 +33,7 @@ TQ_FLAG_SLOT_OUT_OF_RANGE = 1
 TQ_FLAG_BLOCK_OUT_OF_RANGE = 2
 TQ_FLAG_SEQ_TOO_LONG = 4
 TQ_FLAG_WAIT_TIMEOUT = 8
+TQ_RING_TOKENS = 128  # include/tq.h
 
 _PKG = Path(__file__).resolve().parent
 
@@ -111,6 +113,20 @@ _SIGNATURES = {
                                                    ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
                                                    ctypes.c_float, ctypes.c_int32, ctypes.c_void_p,
                                                    ctypes.c_void_p]),
+    "tq_ring_workspace_size": (ctypes.c_size_t, [ctypes.c_int32]),
+    "tq_ring_append": (ctypes.c_int, [ctypes.POINTER(TqConfig), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                      ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(TqCache), ctypes.c_void_p,
+                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "tq_decode_ring_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(TqConfig), ctypes.c_int32, ctypes.c_int32,
+                                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                        ctypes.c_int32]),
+    "tq_decode_attention_ring": (ctypes.c_int, [ctypes.POINTER(TqConfig), ctypes.c_void_p, ctypes.c_int32,
+                                                ctypes.c_int32, ctypes.POINTER(TqCache), ctypes.c_void_p,
+                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_float,
+                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                                ctypes.c_void_p]),
     "tq_hybrid_page": (ctypes.c_int, [ctypes.POINTER(TqConfig), ctypes.c_int32, ctypes.c_int32,
                                       ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
@@ -288,6 +304,70 @@ def tq_decode_attention_noalloc(cfg: TqConfig, q: torch.Tensor, cache: PagedCach
         _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
         _dev(seq_lens, torch.int32, "seq_lens"), int(max_seq_len), float(sm_scale), int(num_splits),
         _dev(out, torch.float32, "out"), _stream(stream)))
+
+
+# -- ring-buffered store ([ART] article, full_tq write path) ------------------------
+
+def new_ring(cfg: TqConfig, num_seqs: int, num_kv_heads: int, ring_tokens: int = TQ_RING_TOKENS,
+             device="cuda"):
+    """(ring_k, ring_v): bf16 [num_seqs, ring_tokens, num_kv_heads, head_dim]."""
+    shape = (num_seqs, ring_tokens, num_kv_heads, cfg.head_dim)
+    return (torch.zeros(shape, dtype=torch.bfloat16, device=device),
+            torch.zeros(shape, dtype=torch.bfloat16, device=device))
+
+
+def tq_ring_workspace_size(num_seqs: int) -> int:
+    return int(lib().tq_ring_workspace_size(num_seqs))
+
+
+def tq_ring_append(cfg: TqConfig, k: torch.Tensor, v: torch.Tensor, cu_new: torch.Tensor, seq_lens: torch.Tensor,
+                   ring_k: torch.Tensor, ring_v: torch.Tensor, cache: PagedCache, block_table: torch.Tensor,
+                   workspace: torch.Tensor, stream=None):
+    """k, v: bf16 [T, H, d] new tokens, sequence s's rows cu_new[s]..cu_new[s+1]-1
+    (int32 [S + 1]); seq_lens int32 [S]: tokens before the call; rings from new_ring."""
+    num_seqs = seq_lens.shape[0]
+    if cu_new.shape != (num_seqs + 1,) or block_table.dim() != 2 or block_table.shape[0] != num_seqs:
+        raise ValueError("cu_new must be [S + 1] and block_table [S, max_blocks]")
+    if ring_k.shape != ring_v.shape or ring_k.dim() != 4 or ring_k.shape[0] != num_seqs:
+        raise ValueError("ring_k and ring_v must be [S, R, H, d]")
+    desc = cache.descriptor()
+    _check(lib().tq_ring_append(
+        ctypes.byref(cfg), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"), k.shape[0],
+        _dev(cu_new, torch.int32, "cu_new"), num_seqs, _dev(seq_lens, torch.int32, "seq_lens"),
+        _dev(ring_k, torch.bfloat16, "ring_k"), _dev(ring_v, torch.bfloat16, "ring_v"), ring_k.shape[1],
+        ctypes.byref(desc), _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def tq_decode_ring_workspace_size(cfg: TqConfig, num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                  block_size: int, max_seq_len: int, num_splits: int = 0) -> int:
+    n = lib().tq_decode_ring_workspace_size(ctypes.byref(cfg), num_seqs, num_q_heads, num_kv_heads, block_size,
+                                            max_seq_len, num_splits)
+    if n == 0:
+        raise TQError(1, "invalid decode sizes")
+    return int(n)
+
+
+def tq_decode_attention_ring(cfg: TqConfig, q: torch.Tensor, cache: PagedCache, block_table: torch.Tensor,
+                             seq_lens: torch.Tensor, max_seq_len: int, ring_k: torch.Tensor, ring_v: torch.Tensor,
+                             out: torch.Tensor, workspace: torch.Tensor, sm_scale: float = 0.0, num_splits: int = 0,
+                             stream=None):
+    """Decode over the packed whole ring blocks plus the exact ring rows;
+    seq_lens counts both (tq_decode_attention_ring in include/tq.h)."""
+    if q.dim() != 3 or q.shape[2] != cfg.head_dim or out.shape != q.shape:
+        raise ValueError("q and out must be [num_seqs, num_q_heads, head_dim]")
+    if block_table.dim() != 2 or block_table.shape[0] != q.shape[0] or seq_lens.shape != (q.shape[0],):
+        raise ValueError("block_table must be [S, max_blocks] and seq_lens [S]")
+    if ring_k.shape != ring_v.shape or ring_k.dim() != 4 or ring_k.shape[0] != q.shape[0]:
+        raise ValueError("ring_k and ring_v must be [S, R, H, d]")
+    desc = cache.descriptor()
+    _check(lib().tq_decode_attention_ring(
+        ctypes.byref(cfg), _dev(q, torch.bfloat16, "q"), q.shape[0], q.shape[1], ctypes.byref(desc),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _dev(seq_lens, torch.int32, "seq_lens"), int(max_seq_len), float(sm_scale), int(num_splits),
+        _dev(ring_k, torch.bfloat16, "ring_k"), _dev(ring_v, torch.bfloat16, "ring_v"), ring_k.shape[1],
+        _dev(out, torch.float32, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)))
 
 
 def tq_dequant(cfg: TqConfig, cache: PagedCache, block_table: torch.Tensor, cu_seqlens: torch.Tensor,

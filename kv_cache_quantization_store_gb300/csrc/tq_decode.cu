@@ -39,13 +39,15 @@ struct DecodeArgs {
     const uint16_t* q;
     const int32_t* block_table;
     const int32_t* seq_lens;
-    float* partials;  // [S, Hq, splits, D + 2]
+    float* partials;  // [S, Hq, slot_stride, D + 2]
     int num_q_heads;
     int max_blocks;
     int max_seq_len;
     int chunks_per_split;
     int num_splits;
-    float qscale;  // sm_scale * log2(e)
+    int slot_stride;  // partial slots per (sequence, query head)
+    int ring_tokens;  // > 0: the last L mod ring_tokens tokens are in an exact ring, not in the cache
+    float qscale;     // sm_scale * log2(e)
 };
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
@@ -90,6 +92,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const DecodeArgs a) {
 
     // ---- sequence range ----------------------------------------------------
     int L = a.seq_lens[s];
+    if (a.ring_tokens > 0 && L > 0) L -= L % a.ring_tokens;  // packed positions: the whole ring blocks
     const int cap = min(a.max_seq_len, a.max_blocks * c.block_size);
     if (L > cap || L < 0) {
         if (tid == 0 && split == 0) set_flag(c.flags, kFlagSeq);
@@ -294,7 +297,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const DecodeArgs a) {
         for (int g = 0; g < kMaxG; ++g) {
             if (g < G) {
                 const int hq = h * G + g;
-                float* part = a.partials + ((static_cast<int64_t>(s) * Hq + hq) * a.num_splits + split) * (D + 2);
+                float* part = a.partials + ((static_cast<int64_t>(s) * Hq + hq) * a.slot_stride + split) * (D + 2);
                 if (lane == 0) {
                     part[0] = m_s[hq];
                     part[1] = l_s[hq];
@@ -399,7 +402,7 @@ combine_kernel(const float* __restrict__ partials, float* __restrict__ out, int 
 }
 
 template <int D, int KB, int VB>
-cudaError_t launch(const LayerParams& p, const CacheGeom& c, const DecodeArgs& a, int num_seqs, float* out,
+cudaError_t launch(const LayerParams& p, const CacheGeom& c, const DecodeArgs& a, int num_seqs,
                    cudaStream_t stream) {
     const SmemLayout lay(a.num_q_heads, D, c.num_kv_heads, Slot<D, KB, VB>::kAligned);
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -407,22 +410,134 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const DecodeArgs& a
     if (e != cudaSuccess) return e;
     dim3 grid(static_cast<unsigned>(a.num_splits), static_cast<unsigned>(num_seqs));
     decode_kernel<D, KB, VB><<<grid, kThreads, lay.total, stream>>>(p, c, a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_combine(a.partials, out, num_seqs, a.num_q_heads, D, a.num_splits, stream);
+    return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const DecodeArgs& a, int ns, float* out,
-                          cudaStream_t st) {
+cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const DecodeArgs& a, int ns, cudaStream_t st) {
     const int kb = p.kbits, vb = p.vbits;
-    if (kb == 3 && vb == 3) return launch<D, 3, 3>(p, c, a, ns, out, st);
-    if (kb == 3 && vb == 4) return launch<D, 3, 4>(p, c, a, ns, out, st);
-    if (kb == 4 && vb == 3) return launch<D, 4, 3>(p, c, a, ns, out, st);
-    if (kb == 4 && vb == 4) return launch<D, 4, 4>(p, c, a, ns, out, st);
-    if (kb == 8 && vb == 3) return launch<D, 8, 3>(p, c, a, ns, out, st);
-    if (kb == 8 && vb == 4) return launch<D, 8, 4>(p, c, a, ns, out, st);
+    if (kb == 3 && vb == 3) return launch<D, 3, 3>(p, c, a, ns, st);
+    if (kb == 3 && vb == 4) return launch<D, 3, 4>(p, c, a, ns, st);
+    if (kb == 4 && vb == 3) return launch<D, 4, 3>(p, c, a, ns, st);
+    if (kb == 4 && vb == 4) return launch<D, 4, 4>(p, c, a, ns, st);
+    if (kb == 8 && vb == 3) return launch<D, 8, 3>(p, c, a, ns, st);
+    if (kb == 8 && vb == 4) return launch<D, 8, 4>(p, c, a, ns, st);
     return cudaErrorInvalidValue;
+}
+
+// Partial state of the exact ring rows ([ART] hnwysp.cn article: in the
+// hybrid mode the newest tokens come from the exact ring): for sequence s
+// of L tokens and KV head h, the n = L mod R rows 0 .. n - 1 of the ring
+// (positions R floor(L / R) onward) against the G query heads of h, in the
+// split partials' form (log2-domain running maximum m, l = sum 2^(s - m),
+// o = sum 2^(s - m) v) in partial slot `slot`.  One CTA of kRingThreads per
+// (KV head, sequence): scores by warp reductions over the dims, softmax per
+// query, then one thread per dim accumulates all G queries' outputs.
+constexpr int kRingThreads = 128;
+constexpr int kRingMaxTokens = 128;
+
+template <int D>
+__global__ void __launch_bounds__(kRingThreads)
+ring_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ ring_k,
+                    const uint16_t* __restrict__ ring_v, const int32_t* __restrict__ seq_lens, int R, int H, int Hq,
+                    float qscale, float* __restrict__ partials, int slot_stride, int slot) {
+    constexpr int kWarps = kRingThreads / 32;
+    constexpr int DPL = (D + 31) / 32;  // dims per lane
+    __shared__ float qf[8][D];
+    __shared__ float pr[8][kRingMaxTokens];
+    __shared__ float ms[8], ls[8];
+    const int h = blockIdx.x, s = blockIdx.y;
+    const int G = Hq / H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int L = seq_lens[s];
+    const int n = L > 0 ? L % R : 0;
+    const uint16_t* qs = q + (static_cast<int64_t>(s) * Hq + static_cast<int64_t>(h) * G) * D;
+    for (int i = threadIdx.x; i < G * D; i += kRingThreads)
+        qf[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qs[i]) << 16) * qscale;
+    __syncthreads();
+    const int64_t row_stride = static_cast<int64_t>(H) * D;  // one ring row: all heads
+    const int64_t base = (static_cast<int64_t>(s) * R * H + h) * D;
+    // scores: warp w takes rows w, w + kWarps, ...
+    for (int t = warp; t < n; t += kWarps) {
+        const uint16_t* kr = ring_k + base + t * row_stride;
+        float kd[DPL];
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) {
+            const int dim = lane + 32 * j;
+            kd[j] = dim < D ? __uint_as_float(static_cast<uint32_t>(kr[dim]) << 16) : 0.f;
+        }
+        for (int g = 0; g < G; ++g) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) {
+                const int dim = lane + 32 * j;
+                if (dim < D) acc = fmaf(qf[g][dim], kd[j], acc);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0) pr[g][t] = acc;
+        }
+    }
+    __syncthreads();
+    // softmax per query: warp w takes queries w, w + kWarps, ...
+    for (int g = warp; g < G; g += kWarps) {
+        float m = -INFINITY;
+        for (int t = lane; t < n; t += 32) m = fmaxf(m, pr[g][t]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        for (int t = lane; t < n; t += 32) {
+            const float e = exp2f(pr[g][t] - m);
+            pr[g][t] = e;
+            l += e;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            ms[g] = m;
+            ls[g] = l;
+        }
+    }
+    __syncthreads();
+    for (int dim = threadIdx.x; dim < D; dim += kRingThreads) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int t = 0; t < n; ++t) {
+            const float vv = __uint_as_float(static_cast<uint32_t>(ring_v[base + t * row_stride + dim]) << 16);
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+                if (g < G) acc[g] = fmaf(pr[g][t], vv, acc[g]);
+        }
+        for (int g = 0; g < G; ++g) {
+            float* part = partials + ((static_cast<int64_t>(s) * Hq + h * G + g) * slot_stride + slot) * (D + 2);
+            if (dim == 0) {
+                part[0] = n > 0 ? ms[g] : -INFINITY;
+                part[1] = n > 0 ? ls[g] : 0.f;
+            }
+            part[2 + dim] = acc[g];
+        }
+    }
+}
+
+cudaError_t launch_ring_partial(const LayerParams& p, const uint16_t* q, const RingBuf& ring,
+                                const int32_t* seq_lens, int num_seqs, int H, int Hq, float qscale, float* partials,
+                                int slot_stride, int slot, cudaStream_t stream) {
+    if (ring.tokens <= 0 || ring.tokens > kRingMaxTokens || Hq % H != 0 || Hq / H > 8) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(num_seqs));
+    switch (p.d) {
+#define TQ_RING_CASE(DD)                                                                                  \
+    case DD:                                                                                              \
+        ring_partial_kernel<DD><<<grid, kRingThreads, 0, stream>>>(q, ring.k, ring.v, seq_lens, ring.tokens, \
+                                                                   H, Hq, qscale, partials, slot_stride, slot); \
+        break;
+        TQ_RING_CASE(16)
+        TQ_RING_CASE(32)
+        TQ_RING_CASE(64)
+        TQ_RING_CASE(128)
+        TQ_RING_CASE(256)
+#undef TQ_RING_CASE
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -459,7 +574,7 @@ int v1_ctas_per_sm(const LayerParams& p, int num_kv_heads, int num_q_heads) {
 }
 
 DecodePlan plan_decode(const LayerParams& p, int num_seqs, int num_q_heads, int num_kv_heads, int max_seq_len,
-                       int num_splits_req, int sm_count) {
+                       int num_splits_req, int sm_count, bool ring) {
     DecodePlan plan{};
     const int max_chunks = (max_seq_len + kTokPerChunk - 1) / kTokPerChunk;
     int splits = 1;
@@ -492,7 +607,9 @@ DecodePlan plan_decode(const LayerParams& p, int num_seqs, int num_q_heads, int 
     if (cps > 0) splits = (max_chunks + cps - 1) / cps;
     plan.num_splits = splits;
     plan.chunks_per_split = cps;
-    plan.partial_bytes = static_cast<size_t>(num_seqs) * num_q_heads * splits * (p.d + 2) * sizeof(float);
+    plan.slot_stride = splits + (ring ? 1 : 0);
+    plan.partial_bytes =
+        static_cast<size_t>(num_seqs) * num_q_heads * plan.slot_stride * (p.d + 2) * sizeof(float);
     plan.workspace_bytes = (plan.partial_bytes + 255) & ~static_cast<size_t>(255);
     if (plan.workspace_bytes == 0) plan.workspace_bytes = 256;
     return plan;
@@ -501,29 +618,43 @@ DecodePlan plan_decode(const LayerParams& p, int num_seqs, int num_q_heads, int 
 cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16_t* q, int num_seqs,
                           int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
                           const int32_t* seq_lens, int max_seq_len, float sm_scale, const DecodePlan& plan,
-                          float* out, void* workspace, cudaStream_t stream) {
-    if (decode_mma_supported(p, c.num_kv_heads, num_q_heads))
-        return launch_decode_mma(p, c, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq, seq_lens,
-                                 max_seq_len, sm_scale, plan, out, workspace, stream);
-    DecodeArgs a{};
-    a.q = q;
-    a.block_table = block_table;
-    a.seq_lens = seq_lens;
-    a.partials = static_cast<float*>(workspace);
-    a.num_q_heads = num_q_heads;
-    a.max_blocks = max_blocks_per_seq;
-    a.max_seq_len = max_seq_len;
-    a.chunks_per_split = plan.chunks_per_split;
-    a.num_splits = plan.num_splits;
-    a.qscale = sm_scale * kLog2e;
-    switch (p.d) {
-        case 16: return dispatch_bits<16>(p, c, a, num_seqs, out, stream);
-        case 32: return dispatch_bits<32>(p, c, a, num_seqs, out, stream);
-        case 64: return dispatch_bits<64>(p, c, a, num_seqs, out, stream);
-        case 128: return dispatch_bits<128>(p, c, a, num_seqs, out, stream);
-        case 256: return dispatch_bits<256>(p, c, a, num_seqs, out, stream);
-        default: return cudaErrorInvalidValue;
+                          const RingBuf& ring, float* out, void* workspace, cudaStream_t stream) {
+    cudaError_t e;
+    if (decode_mma_supported(p, c.num_kv_heads, num_q_heads)) {
+        e = launch_decode_mma(p, c, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq, seq_lens, max_seq_len,
+                              sm_scale, plan, ring.tokens, workspace, stream);
+    } else {
+        DecodeArgs a{};
+        a.q = q;
+        a.block_table = block_table;
+        a.seq_lens = seq_lens;
+        a.partials = static_cast<float*>(workspace);
+        a.num_q_heads = num_q_heads;
+        a.max_blocks = max_blocks_per_seq;
+        a.max_seq_len = max_seq_len;
+        a.chunks_per_split = plan.chunks_per_split;
+        a.num_splits = plan.num_splits;
+        a.slot_stride = plan.slot_stride;
+        a.ring_tokens = ring.tokens;
+        a.qscale = sm_scale * kLog2e;
+        switch (p.d) {
+            case 16: e = dispatch_bits<16>(p, c, a, num_seqs, stream); break;
+            case 32: e = dispatch_bits<32>(p, c, a, num_seqs, stream); break;
+            case 64: e = dispatch_bits<64>(p, c, a, num_seqs, stream); break;
+            case 128: e = dispatch_bits<128>(p, c, a, num_seqs, stream); break;
+            case 256: e = dispatch_bits<256>(p, c, a, num_seqs, stream); break;
+            default: e = cudaErrorInvalidValue; break;
+        }
     }
+    if (e != cudaSuccess) return e;
+    float* partials = static_cast<float*>(workspace);
+    if (ring.tokens > 0) {
+        if (plan.slot_stride != plan.num_splits + 1) return cudaErrorInvalidValue;
+        e = launch_ring_partial(p, q, ring, seq_lens, num_seqs, c.num_kv_heads, num_q_heads, sm_scale * kLog2e,
+                                partials, plan.slot_stride, plan.num_splits, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_combine(partials, out, num_seqs, num_q_heads, p.d, plan.slot_stride, stream);
 }
 
 }  // namespace tq

@@ -1,6 +1,6 @@
 // Host side of the tensor-core decode: shape support, the centroid table
-// scale, occupancy queries and the launch (split kernel, then the combine
-// kernel of tq_decode.cu).  The kernel itself is in tq_decode_mma.cuh.
+// scale, occupancy queries and the launch of the split kernel (tq_decode.cu
+// merges the partials).  The kernel itself is in tq_decode_mma.cuh.
 #include <cmath>
 #include <mutex>
 
@@ -76,7 +76,7 @@ int decode_mma_ctas_per_sm(const LayerParams& p, int num_kv_heads, int num_q_hea
 cudaError_t launch_decode_mma(const LayerParams& p, const CacheGeom& c, const uint16_t* q, int num_seqs,
                               int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
                               const int32_t* seq_lens, int max_seq_len, float sm_scale, const DecodePlan& plan,
-                              float* out, void* workspace, cudaStream_t stream) {
+                              int ring_tokens, void* workspace, cudaStream_t stream) {
     mma::Args a{};
     a.q = q;
     a.block_table = block_table;
@@ -87,11 +87,11 @@ cudaError_t launch_decode_mma(const LayerParams& p, const CacheGeom& c, const ui
     a.max_seq_len = max_seq_len;
     a.chunks_per_split = plan.chunks_per_split;
     a.num_splits = plan.num_splits;
+    a.slot_stride = plan.slot_stride;
+    a.ring_tokens = ring_tokens;
     a.qscale = sm_scale * mma::kLog2e;
     a.lut_scale = table_gamma(p) * sqrtf(static_cast<float>(p.d));
-    const cudaError_t e = run(p, c, a, num_seqs, c.num_kv_heads, stream, nullptr);
-    if (e != cudaSuccess) return e;
-    return launch_combine(a.partials, out, num_seqs, num_q_heads, p.d, a.num_splits, stream);
+    return run(p, c, a, num_seqs, c.num_kv_heads, stream, nullptr);
 }
 
 }  // namespace tq

@@ -66,6 +66,8 @@ struct Args {
     int max_seq_len;
     int chunks_per_split;
     int num_splits;
+    int slot_stride;  // partial slots per (sequence, query head)
+    int ring_tokens;  // > 0: the last L mod ring_tokens tokens are in an exact ring, not in the cache
     float qscale;     // sm_scale * log2(e)
     float lut_scale;  // table value = centroid * lut_scale (= gamma * sqrt(d))
     int tok_eo;       // token order of the chunk rows: 0 natural, 1 even tokens then odd tokens
@@ -260,6 +262,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 
     // ---- sequence range ------------------------------------------------------
     int L = a.seq_lens[s];
+    if (a.ring_tokens > 0 && L > 0) L -= L % a.ring_tokens;  // packed positions: the whole ring blocks
     const int cap = min(a.max_seq_len, a.max_blocks * c.block_size);
     if (L > cap || L < 0) {
         if (threadIdx.x == 0 && split == 0) set_flag(c.flags, kFlagSeq);
@@ -819,7 +822,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         const int q = 2 * cc + e;
         if (q >= Gq) continue;
         const int hq = h * Gq + q;
-        float* part_out = a.partials + ((static_cast<int64_t>(s) * Hq + hq) * a.num_splits + split) * (D + 2);
+        float* part_out = a.partials + ((static_cast<int64_t>(s) * Hq + hq) * a.slot_stride + split) * (D + 2);
         if (r == 0 && part == 0) {
             part_out[0] = m_ref[e];
             part_out[1] = l_acc[e];

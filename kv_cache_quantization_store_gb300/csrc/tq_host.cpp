@@ -301,10 +301,12 @@ size_t tq_decode_workspace_size(const tq_config* cfg, int32_t num_seqs, int32_t 
     return tq::plan_decode(lp, num_seqs, num_q_heads, num_kv_heads, max_seq_len, num_splits, sms).workspace_bytes;
 }
 
-tq_status tq_decode_attention(const tq_config* cfg, const void* q_dev, int32_t num_seqs, int32_t num_q_heads,
-                              const tq_cache* cache, const int32_t* block_table_dev, int32_t max_blocks_per_seq,
-                              const int32_t* seq_lens_dev, int32_t max_seq_len, float sm_scale, int32_t num_splits,
-                              float* out_dev, void* workspace_dev, size_t workspace_bytes, void* stream) {
+namespace {
+tq_status decode_common(const tq_config* cfg, const void* q_dev, int32_t num_seqs, int32_t num_q_heads,
+                        const tq_cache* cache, const int32_t* block_table_dev, int32_t max_blocks_per_seq,
+                        const int32_t* seq_lens_dev, int32_t max_seq_len, float sm_scale, int32_t num_splits,
+                        const tq::RingBuf& ring, float* out_dev, void* workspace_dev, size_t workspace_bytes,
+                        void* stream) {
     if (cache == nullptr) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
     tq::LayerParams lp;
     tq_status st = layer_params(cfg, cache->layer_idx, &lp);
@@ -329,7 +331,8 @@ tq_status tq_decode_attention(const tq_config* cfg, const void* q_dev, int32_t n
     st = sm_count(&sms);
     if (st != TQ_OK) return st;
     const tq::DecodePlan plan =
-        tq::plan_decode(lp, num_seqs, num_q_heads, cache->num_kv_heads, max_seq_len, num_splits, sms);
+        tq::plan_decode(lp, num_seqs, num_q_heads, cache->num_kv_heads, max_seq_len, num_splits, sms,
+                        ring.tokens > 0);
     if (workspace_dev == nullptr || workspace_bytes < plan.workspace_bytes)
         return fail(TQ_ERR_WORKSPACE, "decode workspace needs %zu bytes (got %zu)", plan.workspace_bytes,
                     workspace_bytes);
@@ -337,8 +340,93 @@ tq_status tq_decode_attention(const tq_config* cfg, const void* q_dev, int32_t n
     const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(cfg->head_dim));
     const cudaError_t e = tq::launch_decode(lp, g, static_cast<const uint16_t*>(q_dev), num_seqs, num_q_heads,
                                             block_table_dev, max_blocks_per_seq, seq_lens_dev, max_seq_len, scale,
-                                            plan, out_dev, workspace_dev, static_cast<cudaStream_t>(stream));
+                                            plan, ring, out_dev, workspace_dev, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tq_decode_attention launch");
+    return TQ_OK;
+}
+}  // namespace
+
+tq_status tq_decode_attention(const tq_config* cfg, const void* q_dev, int32_t num_seqs, int32_t num_q_heads,
+                              const tq_cache* cache, const int32_t* block_table_dev, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens_dev, int32_t max_seq_len, float sm_scale, int32_t num_splits,
+                              float* out_dev, void* workspace_dev, size_t workspace_bytes, void* stream) {
+    return decode_common(cfg, q_dev, num_seqs, num_q_heads, cache, block_table_dev, max_blocks_per_seq, seq_lens_dev,
+                         max_seq_len, sm_scale, num_splits, tq::RingBuf{nullptr, nullptr, 0}, out_dev, workspace_dev,
+                         workspace_bytes, stream);
+}
+
+size_t tq_decode_ring_workspace_size(const tq_config* cfg, int32_t num_seqs, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t block_size, int32_t max_seq_len,
+                                     int32_t num_splits) {
+    (void)block_size;
+    tq::LayerParams lp;
+    if (layer_params(cfg, 0, &lp) != TQ_OK) return 0;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0) return 0;
+    int sms = 1;
+    if (num_splits <= 0 && sm_count(&sms) != TQ_OK) return 0;
+    return tq::plan_decode(lp, num_seqs, num_q_heads, num_kv_heads, max_seq_len, num_splits, sms, true)
+        .workspace_bytes;
+}
+
+tq_status tq_decode_attention_ring(const tq_config* cfg, const void* q_dev, int32_t num_seqs, int32_t num_q_heads,
+                                   const tq_cache* cache, const int32_t* block_table_dev,
+                                   int32_t max_blocks_per_seq, const int32_t* seq_lens_dev, int32_t max_seq_len,
+                                   float sm_scale, int32_t num_splits, const void* ring_k_dev,
+                                   const void* ring_v_dev, int32_t ring_tokens, float* out_dev, void* workspace_dev,
+                                   size_t workspace_bytes, void* stream) {
+    if (ring_tokens < 1 || ring_tokens > TQ_RING_MAX_TOKENS)
+        return fail(TQ_ERR_UNSUPPORTED, "ring_tokens must be in [1, %d] (got %d)", TQ_RING_MAX_TOKENS, ring_tokens);
+    if (num_seqs > 0 && (ring_k_dev == nullptr || ring_v_dev == nullptr))
+        return fail(TQ_ERR_INVALID_ARG, "ring_k and ring_v must not be NULL");
+    if (!aligned(ring_k_dev, 4) || !aligned(ring_v_dev, 4))
+        return fail(TQ_ERR_INVALID_ARG, "ring_k and ring_v must be 4-byte aligned");
+    if (cache != nullptr && (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0 ||
+                             num_q_heads / cache->num_kv_heads > 8))
+        return fail(TQ_ERR_UNSUPPORTED, "the ring decode supports up to 8 query heads per KV head");
+    const tq::RingBuf ring{static_cast<const uint16_t*>(ring_k_dev), static_cast<const uint16_t*>(ring_v_dev),
+                           ring_tokens};
+    return decode_common(cfg, q_dev, num_seqs, num_q_heads, cache, block_table_dev, max_blocks_per_seq, seq_lens_dev,
+                         max_seq_len, sm_scale, num_splits, ring, out_dev, workspace_dev, workspace_bytes, stream);
+}
+
+size_t tq_ring_workspace_size(int32_t num_seqs) { return num_seqs < 0 ? 0 : tq::ring_workspace_bytes(num_seqs); }
+
+tq_status tq_ring_append(const tq_config* cfg, const void* k_dev, const void* v_dev, int64_t num_tokens,
+                         const int32_t* cu_new_dev, int32_t num_seqs, const int32_t* seq_lens_dev, void* ring_k_dev,
+                         void* ring_v_dev, int32_t ring_tokens, const tq_cache* cache,
+                         const int32_t* block_table_dev, int32_t max_blocks_per_seq, void* workspace_dev,
+                         size_t workspace_bytes, void* stream) {
+    if (cache == nullptr) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
+    tq::LayerParams lp;
+    tq_status st = layer_params(cfg, cache->layer_idx, &lp);
+    if (st != TQ_OK) return st;
+    tq::CacheGeom g;
+    st = cache_geom(cache, cfg, false, &g);
+    if (st != TQ_OK) return st;
+    if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq <= 0)
+        return fail(TQ_ERR_INVALID_ARG, "negative size argument");
+    if (ring_tokens < 1 || ring_tokens > TQ_RING_MAX_TOKENS)
+        return fail(TQ_ERR_UNSUPPORTED, "ring_tokens must be in [1, %d] (got %d)", TQ_RING_MAX_TOKENS, ring_tokens);
+    if (num_seqs == 0) return TQ_OK;
+    if (cu_new_dev == nullptr || seq_lens_dev == nullptr || ring_k_dev == nullptr || ring_v_dev == nullptr ||
+        block_table_dev == nullptr || (num_tokens > 0 && (k_dev == nullptr || v_dev == nullptr)))
+        return fail(TQ_ERR_INVALID_ARG, "k, v, cu_new, seq_lens, rings and block_table must not be NULL");
+    if (!aligned(k_dev, 16) || !aligned(v_dev, 16) || !aligned(ring_k_dev, 16) || !aligned(ring_v_dev, 16))
+        return fail(TQ_ERR_INVALID_ARG, "k, v, ring_k and ring_v must be 16-byte aligned");
+    if (!aligned(cu_new_dev, 4) || !aligned(seq_lens_dev, 4) || !aligned(block_table_dev, 4))
+        return fail(TQ_ERR_INVALID_ARG, "cu_new, seq_lens and block_table must be 4-byte aligned");
+    if (workspace_dev == nullptr || workspace_bytes < tq::ring_workspace_bytes(num_seqs))
+        return fail(TQ_ERR_WORKSPACE, "ring append workspace needs %zu bytes (got %zu)",
+                    tq::ring_workspace_bytes(num_seqs), workspace_bytes);
+    if (!aligned(workspace_dev, 16)) return fail(TQ_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    int sms = 0;
+    st = sm_count(&sms);
+    if (st != TQ_OK) return st;
+    const cudaError_t e = tq::launch_ring_append(
+        lp, g, static_cast<const uint16_t*>(k_dev), static_cast<const uint16_t*>(v_dev), num_tokens, cu_new_dev,
+        num_seqs, seq_lens_dev, static_cast<uint16_t*>(ring_k_dev), static_cast<uint16_t*>(ring_v_dev), ring_tokens,
+        block_table_dev, max_blocks_per_seq, workspace_dev, sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tq_ring_append launch");
     return TQ_OK;
 }
 

@@ -74,11 +74,37 @@ __device__ __forceinline__ uint64_t pack8(const uint32_t* code) {
     return w;
 }
 
-template <int D, int KB, int VB>
+// Token map of a ring append ([ART] hnwysp.cn article, "full_tq
+// zero-allocation mode", item 3: new tokens wait in an exact bf16 ring and a
+// ring block is compressed once it is whole).  Sequence s packs the
+// positions [R floor(L/R), R floor((L + N)/R)) (L = seq_lens[s] tokens before
+// the call, N new ones); token t of the append list is position
+// R floor(L/R) + t - off[s] of the sequence with off[s] <= t < off[s + 1],
+// read from ring row p mod R (p < L) or from new row cu_new[s] + p - L.
+struct RingMap {
+    const int64_t* off;  // [num_seqs + 1]: exclusive scan of the packed counts
+    const int32_t* seq_lens;
+    const int32_t* cu_new;
+    const int32_t* block_table;
+    const uint16_t* ring_k;
+    const uint16_t* ring_v;
+    int num_seqs;
+    int ring_tokens;
+    int max_blocks;
+};
+
+// Validity and packed-token count of a sequence's append: L + N must fit the
+// block table (cap tokens) and the new rows the input; otherwise the
+// sequence takes no tokens.
+__device__ __forceinline__ bool ring_seq_ok(int L, int a, int b, int64_t num_tokens, int cap) {
+    return L >= 0 && a >= 0 && b >= a && b <= num_tokens && static_cast<int64_t>(L) + (b - a) <= cap;
+}
+
+template <int D, int KB, int VB, bool RING>
 __global__ void __launch_bounds__(kStoreWarps * 32)
 store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict__ k,
-             const uint16_t* __restrict__ v, const int64_t num_tokens,
-             const int64_t* __restrict__ slot_mapping) {
+             const uint16_t* __restrict__ v, int64_t num_tokens,
+             const int64_t* __restrict__ slot_mapping, const RingMap rm) {
     using S = Slot<D, KB, VB>;
     using LS = LaneSplit<D>;
     constexpr int EPL = LS::kEPL, LPV = LS::kLPV, VPW = LS::kVPW;
@@ -89,7 +115,8 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     // MSE keys (arithmetic-heavy) stage the next step's K and V rows in
     // shared memory by bulk copies; FP8 keys (little arithmetic) read them
     // straight from global memory, coalesced 128 bytes per quarter-warp.
-    constexpr bool kPrefetch = KB != 8;
+    // A ring append's tokens come from two places; they are read directly.
+    constexpr bool kPrefetch = KB != 8 && !RING;
 
     // Element layout: lane part p of a vector owns elements 8 (p + LPV j) + e
     // (j < EPL / 8, e < 8) as x[8 j + e].  The Walsh-Hadamard transform
@@ -111,6 +138,10 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     const int part = lane % LPV;
     const int vin = lane / LPV;
     const int H = c.num_kv_heads;
+    if constexpr (RING) {
+        const int64_t listed = rm.off[rm.num_seqs];  // num_tokens: the host's bound
+        num_tokens = listed < num_tokens ? listed : num_tokens;
+    }
     const int64_t num_vecs = num_tokens * H;
 
     // Sign masks, and the positive-half decision thresholds (the grid is
@@ -170,11 +201,43 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
         const bool valid = vi < num_vecs;
         const int64_t vsafe = valid ? vi : num_vecs - 1;
         uint8_t* my_slot = stage + vin * SA;
+        // the vector's K and V rows and its cache slot (-1: none)
+        const uint16_t* krow = k + vsafe * D;
+        const uint16_t* vrow = v + vsafe * D;
+        int64_t slot_id = -1;
+        if constexpr (RING) {
+            const int64_t t = vsafe / H;
+            const int h = static_cast<int>(vsafe - t * H);
+            int lo = 0, hi = rm.num_seqs;  // off[lo] <= t < off[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (rm.off[mid] <= t) lo = mid;
+                else hi = mid;
+            }
+            const int s_ = lo;
+            const int L = rm.seq_lens[s_];
+            const int R = rm.ring_tokens;
+            const int pos = (L / R) * R + static_cast<int>(t - rm.off[s_]);
+            if (pos < L) {
+                const int64_t r = (static_cast<int64_t>(s_) * R + pos % R) * H + h;
+                krow = rm.ring_k + r * D;
+                vrow = rm.ring_v + r * D;
+            } else {
+                const int64_t r = (static_cast<int64_t>(rm.cu_new[s_]) + (pos - L)) * H + h;
+                krow = k + r * D;
+                vrow = v + r * D;
+            }
+            const int b = rm.block_table[static_cast<int64_t>(s_) * rm.max_blocks + pos / c.block_size];
+            if (b >= 0 && b < c.num_blocks) slot_id = static_cast<int64_t>(b) * c.block_size + pos % c.block_size;
+            else if (valid && part == 0 && h == 0) set_flag(c.flags, kFlagBlock);
+        } else {
+            if (valid) slot_id = slot_mapping[vsafe / H];
+        }
         // this lane's groups: 16 bytes at element 8 (part + LPV j) of its vector
         const uint4* ksrc = kPrefetch ? reinterpret_cast<const uint4*>(ring + 2 * sl * kSpan + vin * D) + part
-                                      : reinterpret_cast<const uint4*>(k + vsafe * D) + part;
+                                      : reinterpret_cast<const uint4*>(krow) + part;
         const uint4* vsrc = kPrefetch ? reinterpret_cast<const uint4*>(ring + (2 * sl + 1) * kSpan + vin * D) + part
-                                      : reinterpret_cast<const uint4*>(v + vsafe * D) + part;
+                                      : reinterpret_cast<const uint4*>(vrow) + part;
         // 16-byte group j of K or V: shared memory (staged) or read-only global
         auto ld16 = [&](const uint4* src, int j) -> uint4 { return kPrefetch ? src[LPV * j] : __ldg(src + LPV * j); };
 
@@ -302,7 +365,7 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
         if (valid && part == 0) {
             const int64_t t = vi / H;
             const int h = static_cast<int>(vi - t * H);
-            const int64_t slot = slot_mapping[t];
+            const int64_t slot = slot_id;
             if (slot >= 0) {
                 const int64_t blk = slot / c.block_size;
                 const int64_t pos = slot - blk * c.block_size;
@@ -334,32 +397,138 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
 
 template <int D, int KB, int VB>
 cudaError_t launch(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
-                   int64_t num_tokens, const int64_t* slot_mapping, int sm_count, cudaStream_t stream) {
+                   int64_t num_tokens, const int64_t* slot_mapping, const RingMap* rm, int sm_count,
+                   cudaStream_t stream) {
     constexpr int VPW = LaneSplit<D>::kVPW;
     const int64_t vecs = num_tokens * c.num_kv_heads;
     const int64_t warps = (vecs + VPW - 1) / VPW;
     const int64_t want = (warps + kStoreWarps - 1) / kStoreWarps;
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     const int grid = static_cast<int>(want < cap ? want : cap);
+    if (rm != nullptr) {
+        store_kernel<D, KB, VB, true><<<grid, kStoreWarps * 32, 0, stream>>>(p, c, k, v, num_tokens, nullptr, *rm);
+        return cudaGetLastError();
+    }
     const int ring_bytes = KB != 8 ? kStoreWarps * 4 * VPW * D * 2 : 0;
-    auto kern = store_kernel<D, KB, VB>;
+    auto kern = store_kernel<D, KB, VB, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ring_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kStoreWarps * 32, ring_bytes, stream>>>(p, c, k, v, num_tokens, slot_mapping);
+    kern<<<grid, kStoreWarps * 32, ring_bytes, stream>>>(p, c, k, v, num_tokens, slot_mapping, RingMap{});
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
-                          int64_t n, const int64_t* sm, int sms, cudaStream_t st) {
+                          int64_t n, const int64_t* sm, const RingMap* rm, int sms, cudaStream_t st) {
     const int kb = p.kbits, vb = p.vbits;
-    if (kb == 3 && vb == 3) return launch<D, 3, 3>(p, c, k, v, n, sm, sms, st);
-    if (kb == 3 && vb == 4) return launch<D, 3, 4>(p, c, k, v, n, sm, sms, st);
-    if (kb == 4 && vb == 3) return launch<D, 4, 3>(p, c, k, v, n, sm, sms, st);
-    if (kb == 4 && vb == 4) return launch<D, 4, 4>(p, c, k, v, n, sm, sms, st);
-    if (kb == 8 && vb == 3) return launch<D, 8, 3>(p, c, k, v, n, sm, sms, st);
-    if (kb == 8 && vb == 4) return launch<D, 8, 4>(p, c, k, v, n, sm, sms, st);
+    if (kb == 3 && vb == 3) return launch<D, 3, 3>(p, c, k, v, n, sm, rm, sms, st);
+    if (kb == 3 && vb == 4) return launch<D, 3, 4>(p, c, k, v, n, sm, rm, sms, st);
+    if (kb == 4 && vb == 3) return launch<D, 4, 3>(p, c, k, v, n, sm, rm, sms, st);
+    if (kb == 4 && vb == 4) return launch<D, 4, 4>(p, c, k, v, n, sm, rm, sms, st);
+    if (kb == 8 && vb == 3) return launch<D, 8, 3>(p, c, k, v, n, sm, rm, sms, st);
+    if (kb == 8 && vb == 4) return launch<D, 8, 4>(p, c, k, v, n, sm, rm, sms, st);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t dispatch_d(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
+                       int64_t num_tokens, const int64_t* slot_mapping, const RingMap* rm, int sm_count,
+                       cudaStream_t stream) {
+    switch (p.d) {
+        case 16: return dispatch_bits<16>(p, c, k, v, num_tokens, slot_mapping, rm, sm_count, stream);
+        case 32: return dispatch_bits<32>(p, c, k, v, num_tokens, slot_mapping, rm, sm_count, stream);
+        case 64: return dispatch_bits<64>(p, c, k, v, num_tokens, slot_mapping, rm, sm_count, stream);
+        case 128: return dispatch_bits<128>(p, c, k, v, num_tokens, slot_mapping, rm, sm_count, stream);
+        case 256: return dispatch_bits<256>(p, c, k, v, num_tokens, slot_mapping, rm, sm_count, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ---- ring append: plan and tail copy ------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+
+// One CTA: off[s] = sum over earlier sequences of the positions their
+// append packs (an exclusive scan in chunks of kPlanThreads sequences).
+__global__ void __launch_bounds__(kPlanThreads)
+ring_plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_new, int num_seqs,
+                 int64_t num_tokens, int R, int cap, int64_t* __restrict__ off, uint32_t* flags) {
+    __shared__ int64_t warp_sum[kPlanThreads / 32];
+    __shared__ int64_t carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int c0 = 0; c0 < num_seqs; c0 += kPlanThreads) {
+        const int s = c0 + threadIdx.x;
+        int64_t cnt = 0;
+        if (s < num_seqs) {
+            const int L = seq_lens[s];
+            const int a = cu_new[s], b = cu_new[s + 1];
+            if (ring_seq_ok(L, a, b, num_tokens, cap)) {
+                cnt = static_cast<int64_t>(R) * ((L + (b - a)) / R - L / R);
+            } else if (L >= 0) {
+                set_flag(flags, kFlagSeq);
+            }
+        }
+        // inclusive scan within the warp, then across the warps
+        int64_t x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int64_t w = warp_sum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(kFull, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sum[lane] = w;  // inclusive over the warps
+        }
+        __syncthreads();
+        const int64_t before = carry + (warp > 0 ? warp_sum[warp - 1] : 0) + (x - cnt);
+        if (s < num_seqs) off[s] = before;
+        __syncthreads();
+        if (threadIdx.x == kPlanThreads - 1) carry = before + cnt;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) off[num_seqs] = carry;
+}
+
+// Copies the new tokens that stay in the ring (positions from R floor((L +
+// N)/R) on) into ring row p mod R; one warp per new token, 16-byte units.
+__global__ void __launch_bounds__(256)
+ring_tail_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int64_t num_tokens,
+                 const int32_t* __restrict__ cu_new, int num_seqs, const int32_t* __restrict__ seq_lens, int R,
+                 int cap, int row_elems, uint16_t* __restrict__ ring_k, uint16_t* __restrict__ ring_v) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int units = row_elems / 8;  // 16-byte units of one row
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); i < num_tokens;
+         i += nwarps) {
+        // the sequence whose new rows hold row i: cu_new[lo] <= i < cu_new[hi]
+        int lo = 0, hi = num_seqs;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cu_new[mid] <= i) lo = mid;
+            else hi = mid;
+        }
+        const int L = seq_lens[lo];
+        const int a = cu_new[lo], b = cu_new[lo + 1];
+        if (!ring_seq_ok(L, a, b, num_tokens, cap) || i < a || i >= b) continue;
+        const int pos = L + static_cast<int>(i - a);
+        if (pos < ((L + (b - a)) / R) * R) continue;  // packed by the store
+        const int64_t dst = (static_cast<int64_t>(lo) * R + pos % R) * row_elems;
+        const uint4* ks = reinterpret_cast<const uint4*>(k + i * row_elems);
+        const uint4* vs = reinterpret_cast<const uint4*>(v + i * row_elems);
+        uint4* kd = reinterpret_cast<uint4*>(ring_k + dst);
+        uint4* vd = reinterpret_cast<uint4*>(ring_v + dst);
+        for (int u = lane; u < units; u += 32) {
+            kd[u] = ks[u];
+            vd[u] = vs[u];
+        }
+    }
 }
 
 }  // namespace
@@ -367,14 +536,39 @@ cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const uint16
 cudaError_t launch_store(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
                          int64_t num_tokens, const int64_t* slot_mapping, int sm_count,
                          cudaStream_t stream) {
-    switch (p.d) {
-        case 16: return dispatch_bits<16>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
-        case 32: return dispatch_bits<32>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
-        case 64: return dispatch_bits<64>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
-        case 128: return dispatch_bits<128>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
-        case 256: return dispatch_bits<256>(p, c, k, v, num_tokens, slot_mapping, sm_count, stream);
-        default: return cudaErrorInvalidValue;
+    return dispatch_d(p, c, k, v, num_tokens, slot_mapping, nullptr, sm_count, stream);
+}
+
+size_t ring_workspace_bytes(int num_seqs) {
+    return (static_cast<size_t>(num_seqs > 0 ? num_seqs : 0) + 1) * sizeof(int64_t) + 256;
+}
+
+cudaError_t launch_ring_append(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
+                               int64_t num_tokens, const int32_t* cu_new, int num_seqs, const int32_t* seq_lens,
+                               uint16_t* ring_k, uint16_t* ring_v, int ring_tokens, const int32_t* block_table,
+                               int max_blocks_per_seq, void* workspace, int sm_count, cudaStream_t stream) {
+    if (num_seqs <= 0) return cudaSuccess;
+    const int cap = max_blocks_per_seq * c.block_size;
+    int64_t* off = static_cast<int64_t*>(workspace);
+    ring_plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, cu_new, num_seqs, num_tokens, ring_tokens, cap, off,
+                                                     c.flags);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // every packed position is an old ring row or a new token: at most
+    // num_tokens + num_seqs (R - 1) of them
+    RingMap rm{off, seq_lens, cu_new, block_table, ring_k, ring_v, num_seqs, ring_tokens, max_blocks_per_seq};
+    const int64_t bound = num_tokens + static_cast<int64_t>(num_seqs) * (ring_tokens - 1);
+    e = dispatch_d(p, c, k, v, bound, nullptr, &rm, sm_count, stream);
+    if (e != cudaSuccess) return e;
+    if (num_tokens > 0) {
+        const int64_t want = (num_tokens + 7) / 8;
+        const int64_t cap_ctas = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
+        const int grid = static_cast<int>(want < cap_ctas ? want : cap_ctas);
+        ring_tail_kernel<<<grid, 256, 0, stream>>>(k, v, num_tokens, cu_new, num_seqs, seq_lens, ring_tokens, cap,
+                                                   c.num_kv_heads * p.d, ring_k, ring_v);
+        e = cudaGetLastError();
     }
+    return e;
 }
 
 }  // namespace tq
