@@ -332,6 +332,7 @@ def run_ours(args):
     e2e = run_e2e(args, tq, wl, cfg, caches, k_new, v_new, slots_new, q, table, lens, max_len, ws, outs, stream,
                   packed, dev)
     dq = measure_dequant(tq, wl, cfg, caches[0], table, max_len, dev, stream, peak)
+    ring = measure_ring(tq, wl, cfg, caches[0], table, k_all, v_all, q, max_len, dev, stream)
 
     clk = clocks.summary()
     result = {
@@ -359,6 +360,7 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": n_calls * 3,
         "dequant": dq,
+        "ring": ring,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -409,6 +411,123 @@ def measure_dequant(tq, wl, cfg, cache, table, max_len, dev, stream, peak, reps=
     return {"value": round(bytes_ / us / 1e3, 1), "unit": "GB/s", "frac": round(bytes_ / us / 1e3 / peak, 4),
             "us_per_call": round(us, 2), "tokens": n,
             "bytes_per_call": bytes_, "note": "packed slots read + bf16 K and V written; not part of the timed step"}
+
+
+def measure_ring(tq, wl, cfg, cache, table, k_all, v_all, q, max_len, dev, stream, cycles=2):
+    """Ring-buffered store ([ART] article, full_tq write path), outside the
+    timed step.  Every sequence replays its last R positions as R
+    single-token decode steps through tq_ring_append (the ring's flush
+    rewrites the same packed bytes), against tq_store_kv of the same token
+    per sequence and step; then the ring decode with R/2 exact tokens per
+    sequence against the plain decode of the same lengths."""
+    import torch
+
+    r_len = tq.TQ_RING_TOKENS
+    lens = wl.seq_lens.astype(np.int64)
+    if (lens < r_len).any():
+        return {"skipped": f"sequences shorter than the {r_len}-token ring"}
+    s_n, h, d = wl.num_seqs, wl.num_kv_heads, wl.head_dim
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    start = lens - r_len
+    ring_k, ring_v = tq.new_ring(cfg, s_n, h, r_len, device=dev)
+    ws = torch.empty(tq.tq_ring_workspace_size(s_n), dtype=torch.uint8, device=dev)
+    one_each = torch.arange(s_n + 1, dtype=torch.int32, device=dev)
+    rows = torch.from_numpy(cu[:-1][None, :] + start[None, :] + np.arange(r_len)[:, None]).to(dev)  # [R, S]
+    k_steps, v_steps = k_all[rows], v_all[rows]  # [R, S, H, d]
+    lens_steps = torch.from_numpy((start[None, :] + np.arange(r_len)[:, None]).astype(np.int32)).to(dev)
+    pos = start[None, :] + np.arange(r_len)[:, None]
+    slots_steps = torch.from_numpy(table.cpu().numpy()[np.arange(s_n)[None, :], pos // wl.block_size].astype(np.int64)
+                                   * wl.block_size + pos % wl.block_size).to(dev)
+    # the ring state of a sequence of `start` tokens: positions R floor(start/R) .. start - 1
+    head = start - start % r_len
+    pre_rows = [np.arange(cu[s] + head[s], cu[s] + start[s]) for s in range(s_n)]
+    pre_cu = torch.from_numpy(np.concatenate([[0], np.cumsum([len(r) for r in pre_rows])]).astype(np.int32)).to(dev)
+    pre_idx = torch.from_numpy(np.concatenate(pre_rows).astype(np.int64)).to(dev)
+    pre_k, pre_v = k_all[pre_idx].contiguous(), v_all[pre_idx].contiguous()
+    pre_lens = torch.from_numpy(head.astype(np.int32)).to(dev)
+
+    def refill():
+        tq.tq_ring_append(cfg, pre_k, pre_v, pre_cu, pre_lens, ring_k, ring_v, cache, table, ws, stream=stream)
+
+    def timed(fn, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i, (a, b) in enumerate(ev):
+            a.record(stream)
+            fn(i)
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) * 1e3 for a, b in ev]
+
+    def append(i, st=stream):
+        tq.tq_ring_append(cfg, k_steps[i], v_steps[i], one_each, lens_steps[i], ring_k, ring_v, cache, table, ws,
+                          stream=st)
+
+    def direct(i, st=stream):
+        tq.tq_store_kv(cfg, k_steps[i], v_steps[i], slots_steps[i], cache, stream=st)
+
+    # per-call latency, host launch included (the device work of one step is small)
+    refill()
+    latency_ring = timed(append, r_len)
+    latency_direct = timed(direct, r_len)
+    # device time per step: the R steps of a cycle captured in one CUDA graph
+    graphs = {}
+    try:
+        for name, fn in (("ring", append), ("direct", direct)):
+            refill()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(r_len):
+                    fn(i, None)  # the capture stream
+            graphs[name] = g
+    except RuntimeError as exc:  # report the latency figures alone
+        torch.cuda.synchronize()
+        graphs = {}
+        graph_error = str(exc).splitlines()[0]
+    else:
+        graph_error = None
+    per_step = {"ring": float("nan"), "direct": float("nan")}
+    for name, g in graphs.items():
+        t = []
+        for _ in range(cycles + 1):
+            refill()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b) * 1e3 / r_len)
+        per_step[name] = statistics.median(t[1:])
+    if cache.error_flags():
+        raise RuntimeError(f"cache error flags {cache.error_flags()} after the ring cycles")
+    # decode with half a ring of exact tokens
+    half = r_len // 2
+    refill()
+    for i in range(half):
+        append(i)
+    mid_lens = lens_steps[half]  # start + R/2 tokens per sequence
+    out = torch.empty((s_n, wl.num_q_heads, d), dtype=torch.float32, device=dev)
+    ws_r = torch.zeros(tq.tq_decode_ring_workspace_size(cfg, s_n, wl.num_q_heads, h, wl.block_size, max_len),
+                       dtype=torch.uint8, device=dev)
+    ws_p = torch.zeros(tq.tq_decode_workspace_size(cfg, s_n, wl.num_q_heads, h, wl.block_size, max_len),
+                       dtype=torch.uint8, device=dev)
+    ring_dec = timed(lambda i: tq.tq_decode_attention_ring(cfg, q, cache, table, mid_lens, max_len, ring_k, ring_v,
+                                                           out, ws_r, stream=stream), 12)[2:]
+    plain_dec = timed(lambda i: tq.tq_decode_attention(cfg, q, cache, table, mid_lens, max_len, out, ws_p,
+                                                       stream=stream), 12)[2:]
+    res = {"ring_tokens": r_len, "cycle_steps": r_len,
+            "append_device_us_per_step": round(per_step["ring"], 2),
+            "store_direct_device_us_per_step": round(per_step["direct"], 2),
+            "append_mtok_s": round(s_n / per_step["ring"], 2),
+            "store_direct_mtok_s": round(s_n / per_step["direct"], 2),
+            "append_latency_us_median": round(statistics.median(latency_ring), 2),
+            "store_direct_latency_us_median": round(statistics.median(latency_direct), 2),
+            "decode_ring_us": round(statistics.median(ring_dec), 2),
+            "decode_plain_us": round(statistics.median(plain_dec), 2), "ring_rows_in_decode": half,
+            "note": "one token per sequence per step, device time from a CUDA graph of one ring cycle; "
+                    "not part of the timed step"}
+    if graph_error:
+        res["graph_error"] = graph_error
+    return res
 
 
 def run_e2e(args, tq, wl, cfg, caches, k_new, v_new, slots_new, q, table, lens, max_len, ws, outs, stream,

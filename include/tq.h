@@ -284,9 +284,9 @@ TQ_API size_t tq_decode_ring_workspace_size(const tq_config* cfg, int32_t num_se
  * of a sequence's tokens: the packed positions [0, R floor(L/R)) are read
  * from the cache as tq_decode_attention reads them, and ring rows 0 .. (L
  * mod R) - 1 exactly (fp32 scores and sums); one softmax covers both.
- * Arguments as tq_decode_attention, plus the rings of tq_ring_append and R;
- * workspace >= tq_decode_ring_workspace_size(...).  Up to 8 query heads per
- * KV head.
+ * Arguments as tq_decode_attention, plus the rings of tq_ring_append
+ * (16-byte aligned) and R; workspace >= tq_decode_ring_workspace_size(...).
+ * Up to 8 query heads per KV head.
  */
 TQ_API tq_status tq_decode_attention_ring(const tq_config* cfg, const void* q_dev, int32_t num_seqs,
                                           int32_t num_q_heads, const tq_cache* cache,

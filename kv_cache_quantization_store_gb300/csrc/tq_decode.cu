@@ -17,6 +17,8 @@
 // the splits by log-sum-exp.
 #include <cmath>
 
+#include <mutex>
+
 #include "tq_device.cuh"
 
 namespace tq {
@@ -431,10 +433,23 @@ cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const Decode
 // (positions R floor(L / R) onward) against the G query heads of h, in the
 // split partials' form (log2-domain running maximum m, l = sum 2^(s - m),
 // o = sum 2^(s - m) v) in partial slot `slot`.  One CTA of kRingThreads per
-// (KV head, sequence): scores by warp reductions over the dims, softmax per
-// query, then one thread per dim accumulates all G queries' outputs.
+// (KV head, sequence).  A row is read by D / 8 lanes, 16 bytes each, so a
+// warp instruction covers 256 / D rows; each lane keeps its 8 dims of every
+// query in registers.  Scores: per row, the lanes' partial dot products
+// meet by shuffles; softmax per query over the rows in shared memory; P.V:
+// each lane accumulates its 8 dims of all G outputs over its rows, and the
+// row groups and warps are added through shared memory.
 constexpr int kRingThreads = 128;
 constexpr int kRingMaxTokens = 128;
+
+__device__ __forceinline__ void bf16x8(const uint4 u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kRingThreads)
@@ -442,40 +457,45 @@ ring_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
                     const uint16_t* __restrict__ ring_v, const int32_t* __restrict__ seq_lens, int R, int H, int Hq,
                     float qscale, float* __restrict__ partials, int slot_stride, int slot) {
     constexpr int kWarps = kRingThreads / 32;
-    constexpr int DPL = (D + 31) / 32;  // dims per lane
-    __shared__ float qf[8][D];
+    constexpr int LPT = D / 8;    // lanes per row
+    constexpr int TPW = 32 / LPT; // rows per warp instruction
+    constexpr int kStep = kWarps * TPW;
     __shared__ float pr[8][kRingMaxTokens];
     __shared__ float ms[8], ls[8];
+    __shared__ float red[kWarps][8][D];
     const int h = blockIdx.x, s = blockIdx.y;
     const int G = Hq / H;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane / LPT;  // row of the warp instruction
+    const int u = lane % LPT;    // 16-byte unit: dims 8u .. 8u + 7
     const int L = seq_lens[s];
     const int n = L > 0 ? L % R : 0;
-    const uint16_t* qs = q + (static_cast<int64_t>(s) * Hq + static_cast<int64_t>(h) * G) * D;
-    for (int i = threadIdx.x; i < G * D; i += kRingThreads)
-        qf[i / D][i % D] = __uint_as_float(static_cast<uint32_t>(qs[i]) << 16) * qscale;
-    __syncthreads();
     const int64_t row_stride = static_cast<int64_t>(H) * D;  // one ring row: all heads
-    const int64_t base = (static_cast<int64_t>(s) * R * H + h) * D;
-    // scores: warp w takes rows w, w + kWarps, ...
-    for (int t = warp; t < n; t += kWarps) {
-        const uint16_t* kr = ring_k + base + t * row_stride;
-        float kd[DPL];
+    const int64_t base = (static_cast<int64_t>(s) * R * H + h) * D + 8 * u;
+    // this lane's 8 dims of every query, scaled to log2 units (2-byte loads:
+    // q is only 4-byte aligned)
+    float qv[8][8];
+    const uint16_t* qs = q + (static_cast<int64_t>(s) * Hq + static_cast<int64_t>(h) * G) * D + 8 * u;
 #pragma unroll
-        for (int j = 0; j < DPL; ++j) {
-            const int dim = lane + 32 * j;
-            kd[j] = dim < D ? __uint_as_float(static_cast<uint32_t>(kr[dim]) << 16) : 0.f;
-        }
-        for (int g = 0; g < G; ++g) {
+    for (int g = 0; g < 8; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            qv[g][e] = g < G ? __uint_as_float(static_cast<uint32_t>(qs[g * D + e]) << 16) * qscale : 0.f;
+    // scores
+#pragma unroll 2
+    for (int t0 = warp * TPW; t0 < n; t0 += kStep) {
+        const int t = t0 + sub;
+        float kf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (t < n) bf16x8(*reinterpret_cast<const uint4*>(ring_k + base + t * row_stride), kf);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            if (g >= G) break;
             float acc = 0.f;
 #pragma unroll
-            for (int j = 0; j < DPL; ++j) {
-                const int dim = lane + 32 * j;
-                if (dim < D) acc = fmaf(qf[g][dim], kd[j], acc);
-            }
+            for (int e = 0; e < 8; ++e) acc = fmaf(qv[g][e], kf[e], acc);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0) pr[g][t] = acc;
+            for (int o = LPT / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (u == 0 && t < n) pr[g][t] = acc;
         }
     }
     __syncthreads();
@@ -499,22 +519,53 @@ ring_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
         }
     }
     __syncthreads();
-    for (int dim = threadIdx.x; dim < D; dim += kRingThreads) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int t = 0; t < n; ++t) {
-            const float vv = __uint_as_float(static_cast<uint32_t>(ring_v[base + t * row_stride + dim]) << 16);
+    // P.V over this lane's rows; the accumulators reuse qv
 #pragma unroll
-            for (int g = 0; g < 8; ++g)
-                if (g < G) acc[g] = fmaf(pr[g][t], vv, acc[g]);
-        }
-        for (int g = 0; g < G; ++g) {
-            float* part = partials + ((static_cast<int64_t>(s) * Hq + h * G + g) * slot_stride + slot) * (D + 2);
-            if (dim == 0) {
-                part[0] = n > 0 ? ms[g] : -INFINITY;
-                part[1] = n > 0 ? ls[g] : 0.f;
+    for (int g = 0; g < 8; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qv[g][e] = 0.f;
+#pragma unroll 2
+    for (int t0 = warp * TPW; t0 < n; t0 += kStep) {
+        const int t = t0 + sub;
+        if (t < n) {
+            float vf[8];
+            bf16x8(*reinterpret_cast<const uint4*>(ring_v + base + t * row_stride), vf);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                if (g >= G) break;
+                const float pg = pr[g][t];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qv[g][e] = fmaf(pg, vf[e], qv[g][e]);
             }
-            part[2 + dim] = acc[g];
         }
+    }
+    // add the warp's row groups (lanes u, u + LPT, ...), then the warps
+#pragma unroll
+    for (int o = LPT; o < 32; o <<= 1)
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qv[g][e] += __shfl_xor_sync(0xffffffffu, qv[g][e], o);
+    if (sub == 0) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            if (g >= G) break;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) red[warp][g][8 * u + e] = qv[g][e];
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * D; i += kRingThreads) {
+        const int g = i / D, dim = i % D;
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) o += red[w][g][dim];
+        float* part = partials + ((static_cast<int64_t>(s) * Hq + h * G + g) * slot_stride + slot) * (D + 2);
+        if (dim == 0) {
+            part[0] = n > 0 ? ms[g] : -INFINITY;
+            part[1] = n > 0 ? ls[g] : 0.f;
+        }
+        part[2 + dim] = o;
     }
 }
 
@@ -615,11 +666,61 @@ DecodePlan plan_decode(const LayerParams& p, int num_seqs, int num_q_heads, int 
     return plan;
 }
 
+namespace {
+// A non-blocking stream and two events per device for the ring partial's
+// fork and join, created on first use and kept for the process (the lock
+// keeps concurrent calls from interleaving their record / wait pairs).
+struct Side {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;
+};
+
+cudaError_t side_stream(Side** out) {
+    constexpr int kDevs = 16;
+    static Side sides[kDevs];
+    static std::mutex init_mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kDevs) return cudaErrorInvalidDevice;
+    Side& sd = sides[dev];
+    std::lock_guard<std::mutex> lock(init_mu);
+    if (sd.stream == nullptr) {
+        e = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            sd.stream = nullptr;
+            return e;
+        }
+    }
+    *out = &sd;
+    return cudaSuccess;
+}
+}  // namespace
+
 cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16_t* q, int num_seqs,
                           int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
                           const int32_t* seq_lens, int max_seq_len, float sm_scale, const DecodePlan& plan,
                           const RingBuf& ring, float* out, void* workspace, cudaStream_t stream) {
-    cudaError_t e;
+    float* partials = static_cast<float*>(workspace);
+    // With a ring, the ring rows' partial runs on a side stream next to the
+    // packed decode (it needs only q, the rings and seq_lens): forked before
+    // the decode is enqueued, launched after it, so that its CTAs take the
+    // SM slots the decode leaves free; the combine waits for both.
+    Side* side = nullptr;
+    std::unique_lock<std::mutex> lock;
+    cudaError_t e = cudaSuccess;
+    if (ring.tokens > 0) {
+        if (plan.slot_stride != plan.num_splits + 1) return cudaErrorInvalidValue;
+        e = side_stream(&side);
+        if (e != cudaSuccess) return e;
+        lock = std::unique_lock<std::mutex>(side->mu);
+        e = cudaEventRecord(side->fork, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+        if (e != cudaSuccess) return e;
+    }
     if (decode_mma_supported(p, c.num_kv_heads, num_q_heads)) {
         e = launch_decode_mma(p, c, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq, seq_lens, max_seq_len,
                               sm_scale, plan, ring.tokens, workspace, stream);
@@ -628,7 +729,7 @@ cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16
         a.q = q;
         a.block_table = block_table;
         a.seq_lens = seq_lens;
-        a.partials = static_cast<float*>(workspace);
+        a.partials = partials;
         a.num_q_heads = num_q_heads;
         a.max_blocks = max_blocks_per_seq;
         a.max_seq_len = max_seq_len;
@@ -646,14 +747,17 @@ cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16
             default: e = cudaErrorInvalidValue; break;
         }
     }
-    if (e != cudaSuccess) return e;
-    float* partials = static_cast<float*>(workspace);
-    if (ring.tokens > 0) {
-        if (plan.slot_stride != plan.num_splits + 1) return cudaErrorInvalidValue;
-        e = launch_ring_partial(p, q, ring, seq_lens, num_seqs, c.num_kv_heads, num_q_heads, sm_scale * kLog2e,
-                                partials, plan.slot_stride, plan.num_splits, stream);
-        if (e != cudaSuccess) return e;
+    if (side != nullptr) {
+        // join the side stream even after a failed decode launch
+        cudaError_t er = launch_ring_partial(p, q, ring, seq_lens, num_seqs, c.num_kv_heads, num_q_heads,
+                                             sm_scale * kLog2e, partials, plan.slot_stride, plan.num_splits,
+                                             side->stream);
+        const cudaError_t ej = cudaEventRecord(side->join, side->stream);
+        const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(stream, side->join, 0) : ej;
+        if (er == cudaSuccess) er = ew;
+        if (e == cudaSuccess) e = er;
     }
+    if (e != cudaSuccess) return e;
     return launch_combine(partials, out, num_seqs, num_q_heads, p.d, plan.slot_stride, stream);
 }
 

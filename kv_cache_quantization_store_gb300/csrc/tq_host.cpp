@@ -378,8 +378,8 @@ tq_status tq_decode_attention_ring(const tq_config* cfg, const void* q_dev, int3
         return fail(TQ_ERR_UNSUPPORTED, "ring_tokens must be in [1, %d] (got %d)", TQ_RING_MAX_TOKENS, ring_tokens);
     if (num_seqs > 0 && (ring_k_dev == nullptr || ring_v_dev == nullptr))
         return fail(TQ_ERR_INVALID_ARG, "ring_k and ring_v must not be NULL");
-    if (!aligned(ring_k_dev, 4) || !aligned(ring_v_dev, 4))
-        return fail(TQ_ERR_INVALID_ARG, "ring_k and ring_v must be 4-byte aligned");
+    if (!aligned(ring_k_dev, 16) || !aligned(ring_v_dev, 16))
+        return fail(TQ_ERR_INVALID_ARG, "ring_k and ring_v must be 16-byte aligned");
     if (cache != nullptr && (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0 ||
                              num_q_heads / cache->num_kv_heads > 8))
         return fail(TQ_ERR_UNSUPPORTED, "the ring decode supports up to 8 query heads per KV head");

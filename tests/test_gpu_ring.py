@@ -160,3 +160,52 @@ def test_ring_decode_without_ring_tokens_matches_plain_decode(cuda_device):
     tq.tq_decode_attention(cfg, q, cache, table, lens, 256, o_p, ws, num_splits=2)
     torch.cuda.synchronize()
     np.testing.assert_allclose(o_r.cpu().numpy(), o_p.cpu().numpy(), rtol=0, atol=1e-6)
+
+
+def test_ring_step_in_cuda_graph(cuda_device):
+    """One decode step (ring append, then ring decode, whose ring partial
+    forks onto the library's side stream) captured in a CUDA graph gives
+    the eager results."""
+    wl = W.custom(128, 4, 4, True, 8, 32, 16, [300, 200], 3107)
+    cfg = host_cfg(wl)
+    k_all, v_all = wl.kv()
+    table, nblk = wl.layout()
+    cu = wl.cu_seqlens()
+    gtable = torch.from_numpy(table.astype(np.int32)).to(cuda_device)
+    q = bf16(wl.q(), cuda_device)
+    lens_before = torch.tensor([299, 199], dtype=torch.int32, device=cuda_device)
+    lens_after = lens_before + 1
+    one_each = torch.arange(3, dtype=torch.int32, device=cuda_device)
+    k_step = bf16(k_all[[cu[0] + 299, cu[1] + 199]], cuda_device)
+    v_step = bf16(v_all[[cu[0] + 299, cu[1] + 199]], cuda_device)
+    ws_a = torch.empty(tq.tq_ring_workspace_size(2), dtype=torch.uint8, device=cuda_device)
+    ws_d = torch.zeros(tq.tq_decode_ring_workspace_size(cfg, 2, 32, 8, 16, 300), dtype=torch.uint8,
+                       device=cuda_device)
+
+    def fresh():
+        cache = tq.new_paged_cache(cfg, nblk, 16, 8, 0, device=cuda_device)
+        rk, rv = tq.new_ring(cfg, 2, 8, 128, device=cuda_device)
+        pre = np.concatenate([np.arange(cu[0], cu[0] + 299), np.arange(cu[1], cu[1] + 199)])
+        tq.tq_ring_append(cfg, bf16(k_all[pre], cuda_device), bf16(v_all[pre], cuda_device),
+                          torch.tensor([0, 299, 498], dtype=torch.int32, device=cuda_device),
+                          torch.zeros(2, dtype=torch.int32, device=cuda_device), rk, rv, cache, gtable, ws_a)
+        return cache, rk, rv
+
+    def step(cache, rk, rv, out, stream=None):
+        tq.tq_ring_append(cfg, k_step, v_step, one_each, lens_before, rk, rv, cache, gtable, ws_a, stream=stream)
+        tq.tq_decode_attention_ring(cfg, q, cache, gtable, lens_after, 300, rk, rv, out, ws_d, stream=stream)
+
+    c1, rk1, rv1 = fresh()
+    out_eager = torch.empty((2, 32, 128), dtype=torch.float32, device=cuda_device)
+    step(c1, rk1, rv1, out_eager)
+    c2, rk2, rv2 = fresh()
+    out_graph = torch.full((2, 32, 128), float("nan"), dtype=torch.float32, device=cuda_device)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(c2, rk2, rv2, out_graph)
+    g.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out_graph.cpu().numpy(), out_eager.cpu().numpy())
+    np.testing.assert_array_equal(c2.data.cpu().numpy(), c1.data.cpu().numpy())
+    assert c1.error_flags() == 0 and c2.error_flags() == 0
