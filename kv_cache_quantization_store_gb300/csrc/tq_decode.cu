@@ -433,12 +433,12 @@ cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const Decode
 // (positions R floor(L / R) onward) against the G query heads of h, in the
 // split partials' form (log2-domain running maximum m, l = sum 2^(s - m),
 // o = sum 2^(s - m) v) in partial slot `slot`.  One CTA of kRingThreads per
-// (KV head, sequence).  A row is read by D / 8 lanes, 16 bytes each, so a
-// warp instruction covers 256 / D rows; each lane keeps its 8 dims of every
-// query in registers.  Scores: per row, the lanes' partial dot products
-// meet by shuffles; softmax per query over the rows in shared memory; P.V:
-// each lane accumulates its 8 dims of all G outputs over its rows, and the
-// row groups and warps are added through shared memory.
+// (KV head, sequence).  Scores: a row is read by D / 8 lanes, 16 bytes
+// each, so a warp instruction covers 256 / D rows; each lane keeps its 8
+// dims of every query in registers, and the lanes' partial dot products
+// meet by shuffles.  Softmax per query over the rows in shared memory.
+// P.V: each warp owns a quarter of the dims and accumulates all G outputs
+// over every row.
 constexpr int kRingThreads = 128;
 constexpr int kRingMaxTokens = 128;
 
@@ -462,7 +462,6 @@ ring_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
     constexpr int kStep = kWarps * TPW;
     __shared__ float pr[8][kRingMaxTokens];
     __shared__ float ms[8], ls[8];
-    __shared__ float red[kWarps][8][D];
     const int h = blockIdx.x, s = blockIdx.y;
     const int G = Hq / H;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -481,21 +480,30 @@ ring_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             qv[g][e] = g < G ? __uint_as_float(static_cast<uint32_t>(qs[g * D + e]) << 16) * qscale : 0.f;
-    // scores
-#pragma unroll 2
-    for (int t0 = warp * TPW; t0 < n; t0 += kStep) {
-        const int t = t0 + sub;
-        float kf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (t < n) bf16x8(*reinterpret_cast<const uint4*>(ring_k + base + t * row_stride), kf);
+    // scores: kBatch rows per lane are loaded before any is used
+    constexpr int kBatch = 8;
+    for (int t0 = warp * TPW + sub; t0 - sub < n; t0 += kStep * kBatch) {
+        uint4 raw[kBatch];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            if (g >= G) break;
-            float acc = 0.f;
+        for (int k = 0; k < kBatch; ++k) {
+            const int t = t0 + k * kStep;
+            raw[k] = t < n ? *reinterpret_cast<const uint4*>(ring_k + base + t * row_stride) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc = fmaf(qv[g][e], kf[e], acc);
+        for (int k = 0; k < kBatch; ++k) {
+            const int t = t0 + k * kStep;
+            float kf[8];
+            bf16x8(raw[k], kf);
 #pragma unroll
-            for (int o = LPT / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (u == 0 && t < n) pr[g][t] = acc;
+            for (int g = 0; g < 8; ++g) {
+                if (g >= G) break;
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = fmaf(qv[g][e], kf[e], acc);
+#pragma unroll
+                for (int o = LPT / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (u == 0 && t < n) pr[g][t] = acc;
+            }
         }
     }
     __syncthreads();
@@ -519,17 +527,35 @@ ring_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
         }
     }
     __syncthreads();
-    // P.V over this lane's rows; the accumulators reuse qv
+    // P.V.  Warp w owns dims [w D/4, (w + 1) D/4) of the output and reads
+    // every row's slice of them: PL lanes per row (8 dims each), PT rows per
+    // warp instruction; the PT row groups meet by shuffles.  (d = 16: the
+    // warps split the rows instead and meet in shared memory.)
+    constexpr bool kDimSplit = D / kWarps >= 8;
+    constexpr int PL = kDimSplit ? D / kWarps / 8 : LPT;
+    constexpr int PT = 32 / PL;
+    const int psub = lane / PL, pu = lane % PL;
+    const int dim0 = kDimSplit ? warp * (D / kWarps) + 8 * pu : 8 * u;
+    const int64_t vbase = (static_cast<int64_t>(s) * R * H + h) * D + dim0;
 #pragma unroll
     for (int g = 0; g < 8; ++g)
 #pragma unroll
         for (int e = 0; e < 8; ++e) qv[g][e] = 0.f;
-#pragma unroll 2
-    for (int t0 = warp * TPW; t0 < n; t0 += kStep) {
-        const int t = t0 + sub;
-        if (t < n) {
+    const int t_first = kDimSplit ? psub : warp * TPW + sub;
+    const int t_step = kDimSplit ? PT : kStep;
+    for (int t0 = t_first; t0 < n; t0 += t_step * kBatch) {
+        uint4 raw[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int t = t0 + k * t_step;
+            raw[k] = t < n ? *reinterpret_cast<const uint4*>(ring_v + vbase + t * row_stride) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int t = t0 + k * t_step;
+            if (t >= n) break;
             float vf[8];
-            bf16x8(*reinterpret_cast<const uint4*>(ring_v + base + t * row_stride), vf);
+            bf16x8(raw[k], vf);
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
                 if (g >= G) break;
@@ -539,33 +565,54 @@ ring_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__
             }
         }
     }
-    // add the warp's row groups (lanes u, u + LPT, ...), then the warps
+    // add the row groups of the warp (lanes pu, pu + PL, ...)
 #pragma unroll
-    for (int o = LPT; o < 32; o <<= 1)
+    for (int o = PL; o < 32; o <<= 1)
 #pragma unroll
         for (int g = 0; g < 8; ++g)
 #pragma unroll
             for (int e = 0; e < 8; ++e) qv[g][e] += __shfl_xor_sync(0xffffffffu, qv[g][e], o);
-    if (sub == 0) {
+    auto part_of = [&](int g) -> float* {
+        return partials + ((static_cast<int64_t>(s) * Hq + h * G + g) * slot_stride + slot) * (D + 2);
+    };
+    if constexpr (kDimSplit) {
+        if (psub == 0) {
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            if (g >= G) break;
+            for (int g = 0; g < 8; ++g) {
+                if (g >= G) break;
+                float* part = part_of(g);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) red[warp][g][8 * u + e] = qv[g][e];
+                for (int e = 0; e < 8; ++e) part[2 + dim0 + e] = qv[g][e];
+            }
         }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < G * D; i += kRingThreads) {
-        const int g = i / D, dim = i % D;
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) o += red[w][g][dim];
-        float* part = partials + ((static_cast<int64_t>(s) * Hq + h * G + g) * slot_stride + slot) * (D + 2);
-        if (dim == 0) {
-            part[0] = n > 0 ? ms[g] : -INFINITY;
-            part[1] = n > 0 ? ls[g] : 0.f;
+        if (threadIdx.x < G) {
+            float* part = part_of(threadIdx.x);
+            part[0] = n > 0 ? ms[threadIdx.x] : -INFINITY;
+            part[1] = n > 0 ? ls[threadIdx.x] : 0.f;
         }
-        part[2 + dim] = o;
+    } else {
+        __shared__ float red[kWarps][8][D];
+        if (sub == 0) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                if (g >= G) break;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) red[warp][g][8 * u + e] = qv[g][e];
+            }
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < G * D; i += kRingThreads) {
+            const int g = i / D, dim = i % D;
+            float o = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) o += red[w][g][dim];
+            float* part = part_of(g);
+            if (dim == 0) {
+                part[0] = n > 0 ? ms[g] : -INFINITY;
+                part[1] = n > 0 ? ls[g] : 0.f;
+            }
+            part[2 + dim] = o;
+        }
     }
 }
 
@@ -632,20 +679,27 @@ DecodePlan plan_decode(const LayerParams& p, int num_seqs, int num_q_heads, int 
     if (num_splits_req > 0) {
         splits = num_splits_req;
     } else if (num_seqs > 0 && max_chunks > 0) {
-        // Pick the split count that finishes soonest: CTAs run in waves of
-        // sm_count * (resident CTAs per SM); each CTA costs its chunks plus a
-        // fixed prologue (tables, query rotation) worth about kPrologue chunks.
+        // Pick the split count that finishes soonest.  CTAs run in waves of
+        // sm_count * (resident CTAs per SM); each costs its chunks plus a
+        // fixed prologue (tables, query rotation) worth about kPrologue
+        // chunks.  A last, partial wave with at most one CTA per SM runs
+        // faster (its CTAs share no SM: measured about 1.6x), so it counts
+        // 10/16 of a wave.  Costs are in 1/16 chunk.
         constexpr int kPrologue = 4;
+        const int sms = sm_count > 0 ? sm_count : 1;
         int per_sm = decode_mma_supported(p, num_kv_heads, num_q_heads)
                          ? decode_mma_ctas_per_sm(p, num_kv_heads, num_q_heads)
                          : v1_ctas_per_sm(p, num_kv_heads, num_q_heads);
         if (per_sm < 1) per_sm = 1;
-        const long long capacity = static_cast<long long>(sm_count > 0 ? sm_count : 1) * per_sm;
+        const long long capacity = static_cast<long long>(sms) * per_sm;
         long long best_cost = -1;
         const int limit = max_chunks < 512 ? max_chunks : 512;
         for (int cand = 1; cand <= limit; ++cand) {
-            const long long waves = (static_cast<long long>(num_seqs) * cand + capacity - 1) / capacity;
-            const long long cost = waves * (kPrologue + (max_chunks + cand - 1) / cand);
+            const long long ctas = static_cast<long long>(num_seqs) * cand;
+            const long long full = ctas / capacity, rem = ctas % capacity;
+            const long long len = kPrologue + (max_chunks + cand - 1) / cand;
+            const long long last = rem == 0 ? 0 : (per_sm > 1 && rem <= sms ? 10 : 16);
+            const long long cost = (full * 16 + last) * len;
             if (best_cost < 0 || cost < best_cost) {
                 best_cost = cost;
                 splits = cand;

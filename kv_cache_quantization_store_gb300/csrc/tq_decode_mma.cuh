@@ -295,6 +295,48 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         fence_mbar_init();
     }
 
+    __syncthreads();  // block ids and mbarriers ready
+
+    // ---- chunk staging.  Chunk it (of this split) lives in stage it % NS; one
+    // thread copies all of it (16 token rows of every head, contiguous in the
+    // paged block) with one bulk copy that completes the stage's mbarrier.  A
+    // warp releases a stage once its data is in registers; the last warp to
+    // release it refills it with chunk it + NS.  No CTA-wide barrier in the loop.
+    uint8_t* const ctrl = smem + G::CTRL_OFF;
+    const uint32_t ctrl_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ctrl));
+    auto full_bar = [&](int slot) -> uint32_t { return ctrl_sh + 8u * slot; };
+    auto cnt_addr = [&](int slot) -> uint32_t { return ctrl_sh + 8u * NS + 4u * slot; };
+    int* const stage_blk = reinterpret_cast<int*>(ctrl + 12 * NS);  // block id of the staged chunk, -1: none
+    int* const err_word = reinterpret_cast<int*>(ctrl + 16 * NS);
+    const int cpb = c.block_size / kTok;  // 16-token chunks per paged block
+    const int32_t* bt_row = a.block_table + static_cast<int64_t>(s) * a.max_blocks;
+    const int nch = c1 - c0;
+    const int col0 = c0 / cpb;
+    const int* bt_sm = reinterpret_cast<const int*>(smem + G::BT_OFF);
+    auto issue = [&](int it) {  // one thread
+        const int slot = it % NS;
+        const int cg = c0 + it;
+        const int col = cg / cpb;
+        int b = col - col0 < G::BT_MAX ? bt_sm[col - col0] : bt_row[col];
+        b = (b >= 0 && b < c.num_blocks) ? b : -1;
+        stage_blk[slot] = b;
+        if (b >= 0) {
+            const uint8_t* src =
+                c.data + static_cast<int64_t>(b) * c.block_stride + static_cast<int64_t>(cg - col * cpb) * G::CHUNK;
+            mbar_arrive_tx(full_bar(slot), G::CHUNK);
+            bulk_copy(ring_sh + slot * G::STAGE, src, G::CHUNK, full_bar(slot));
+        } else {
+            mbar_arrive(full_bar(slot));
+        }
+    };
+    // The query rotation borrows the ring's last nq stages as scratch; the
+    // first chunks go into the others before it starts.
+    const int nq = (Hq * D * 4 + G::STAGE - 1) / G::STAGE;
+    const int early = NS - nq > 0 ? NS - nq : 0;
+    if (threadIdx.x == 0) {
+        for (int it = 0; it < early && it < nch; ++it) issue(it);
+    }
+
     // ---- pair lookup table: centroids * lut_scale as fp16, one copy per lane ----
     const float ls = a.lut_scale;
     if constexpr (KB == 3 || KB == 4) {
@@ -317,7 +359,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 
     // ---- queries: q' = Pi q (MSE keys), scaled, into B fragments ---------------
     {
-        float* qs = reinterpret_cast<float*>(ring);
+        float* qs = reinterpret_cast<float*>(ring + early * G::STAGE);
         const uint16_t* qg = a.q + static_cast<int64_t>(s) * Hq * D;
         for (int i = threadIdx.x; i < Hq * D; i += NT) {
             float x = __uint_as_float(static_cast<uint32_t>(qg[i]) << 16);
@@ -328,18 +370,38 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
             qs[i] = x;
         }
         if constexpr (KB != 8) {
-#pragma unroll 1
-            for (int st = 1; st < D; st <<= 1) {
-                __syncthreads();
-                for (int b = threadIdx.x; b < Hq * D / 2; b += NT) {
-                    const int row = b / (D / 2);
-                    const int j = b % (D / 2);
-                    const int i = (j / st) * 2 * st + (j % st);
-                    float* rw = qs + row * D;
-                    const float x0 = rw[i], x1 = rw[i + st];
-                    rw[i] = x0 + x1;
-                    rw[i + st] = x0 - x1;
+            // Walsh-Hadamard butterflies of each query row in one warp: lane
+            // holds elements lane + 32 j, so the stages 1 .. 16 pair lanes
+            // (shuffles) and 32 .. D/2 pair registers, in the natural stage
+            // order and with the one rounding of each add or subtract.
+            constexpr int E = D / 32;
+            __syncthreads();
+            for (int row = warp; row < Hq; row += G::NWARPS) {
+                float* rw = qs + row * D;
+                float x[E];
+#pragma unroll
+                for (int j = 0; j < E; ++j) x[j] = rw[lane + 32 * j];
+#pragma unroll
+                for (int st = 1; st < 32; st <<= 1) {
+#pragma unroll
+                    for (int j = 0; j < E; ++j) {
+                        const float o = __shfl_xor_sync(kFull, x[j], st);
+                        x[j] = (lane & st) ? o - x[j] : x[j] + o;
+                    }
                 }
+#pragma unroll
+                for (int st = 1; st < E; st <<= 1) {
+#pragma unroll
+                    for (int j = 0; j < E; ++j) {
+                        if ((j & st) == 0) {
+                            const float x0 = x[j], x1 = x[j + st];
+                            x[j] = x0 + x1;
+                            x[j + st] = x0 - x1;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < E; ++j) rw[lane + 32 * j] = x[j];
             }
         }
         __syncthreads();
@@ -389,6 +451,10 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         if (threadIdx.x == 0) *reinterpret_cast<uint4*>(smem + G::ZERO_OFF) = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
     }
+    if (threadIdx.x == 0) {
+        fence_proxy_async();  // the borrowed stages held the rotation (generic proxy writes)
+        for (int it = early; it < NS && it < nch; ++it) issue(it);
+    }
     // lanes of padded query rows (r >= G) read the zero block at every k-step
     const bool q_real = r < Gq;
     const uint4* qfrag = q_real ? reinterpret_cast<const uint4*>(smem + G::q_off(Hq)) + warp * G::KSTEPS * Gq * 4 +
@@ -396,43 +462,6 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
                                 : reinterpret_cast<const uint4*>(smem + G::ZERO_OFF);
     const int qstride = q_real ? Gq * 4 : 0;
     const uint2* qfrag2 = reinterpret_cast<const uint2*>(smem + G::q_off(Hq)) + warp * G::KSTEPS * 32 + lane;
-
-    // ---- chunk staging.  Chunk it (of this split) lives in stage it % NS; one
-    // thread copies all of it (16 token rows of every head, contiguous in the
-    // paged block) with one bulk copy that completes the stage's mbarrier.  A
-    // warp releases a stage once its data is in registers; the last warp to
-    // release it refills it with chunk it + NS.  No CTA-wide barrier in the loop.
-    uint8_t* const ctrl = smem + G::CTRL_OFF;
-    const uint32_t ctrl_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ctrl));
-    auto full_bar = [&](int slot) -> uint32_t { return ctrl_sh + 8u * slot; };
-    auto cnt_addr = [&](int slot) -> uint32_t { return ctrl_sh + 8u * NS + 4u * slot; };
-    int* const stage_blk = reinterpret_cast<int*>(ctrl + 12 * NS);  // block id of the staged chunk, -1: none
-    int* const err_word = reinterpret_cast<int*>(ctrl + 16 * NS);
-    const int cpb = c.block_size / kTok;  // 16-token chunks per paged block
-    const int32_t* bt_row = a.block_table + static_cast<int64_t>(s) * a.max_blocks;
-    const int nch = c1 - c0;
-    const int col0 = c0 / cpb;
-    const int* bt_sm = reinterpret_cast<const int*>(smem + G::BT_OFF);
-    auto issue = [&](int it) {  // one thread
-        const int slot = it % NS;
-        const int cg = c0 + it;
-        const int col = cg / cpb;
-        int b = col - col0 < G::BT_MAX ? bt_sm[col - col0] : bt_row[col];
-        b = (b >= 0 && b < c.num_blocks) ? b : -1;
-        stage_blk[slot] = b;
-        if (b >= 0) {
-            const uint8_t* src =
-                c.data + static_cast<int64_t>(b) * c.block_stride + static_cast<int64_t>(cg - col * cpb) * G::CHUNK;
-            mbar_arrive_tx(full_bar(slot), G::CHUNK);
-            bulk_copy(ring_sh + slot * G::STAGE, src, G::CHUNK, full_bar(slot));
-        } else {
-            mbar_arrive(full_bar(slot));
-        }
-    };
-    if (threadIdx.x == 0) {
-        fence_proxy_async();  // the ring held the query rotation (generic proxy writes)
-        for (int it = 0; it < NS && it < nch; ++it) issue(it);
-    }
 
     // ---- per-thread constant offsets inside a stage.  Row k of the MMA tiles
     // holds token sig(k) of the chunk; the order is chosen on the host to
