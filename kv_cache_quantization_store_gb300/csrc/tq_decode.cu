@@ -312,24 +312,39 @@ decode_kernel(const LayerParams p, const CacheGeom c, const DecodeArgs a) {
 }
 
 // Log-sum-exp merge of the split partials: one CTA per (query head,
-// sequence) with nw warps (nw grows with the split count).  Warp w merges
-// splits w, w + nw, ... on its own: its lanes first fold the splits' (m, l)
-// with a running maximum, then sum the weighted o over those splits (two
-// dims per lane and load, the splits' loads independent of one another).
-// With several warps their (m, l, o) meet in shared memory.
+// sequence) with nw warps (nw grows with the split count), or, for up to
+// 8 splits, one warp per (sequence, query head) and 8 of them per CTA.
+// Warp w merges splits w, w + nw, ... on its own: its lanes first fold the
+// splits' (m, l) with a running maximum, then sum the weighted o over those
+// splits (two dims per lane and load, the splits' loads independent of one
+// another).  With several warps their (m, l, o) meet in shared memory.
 constexpr int kCombineMaxWarps = 8;
 
 // 2^(m - M), 0 for a split without tokens (m = -inf)
 __device__ __forceinline__ float lse_weight(float m, float M) { return m == -INFINITY ? 0.f : exp2f(m - M); }
 
 __global__ void __launch_bounds__(32 * kCombineMaxWarps)
-combine_kernel(const float* __restrict__ partials, float* __restrict__ out, int Hq, int D, int num_splits) {
+combine_kernel(const float* __restrict__ partials, float* __restrict__ out, int num_seqs, int Hq, int D,
+               int num_splits, int one_warp) {
     __shared__ float wm[kCombineMaxWarps], wl[kCombineMaxWarps];
     __shared__ float wacc[kCombineMaxWarps][256];
-    const int hq = blockIdx.x, s = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    int warp = threadIdx.x >> 5, nw = blockDim.x >> 5, hq, s;
+    if (one_warp) {
+        // few splits: each warp merges one (sequence, query head) on its own
+        const int pair = blockIdx.x * nw + warp;
+        if (pair >= num_seqs * Hq) return;
+        s = pair / Hq;
+        hq = pair - s * Hq;
+        warp = 0;
+        nw = 1;
+    } else {
+        hq = blockIdx.x;
+        s = blockIdx.y;
+    }
+    grid_dependency_wait();  // the decode grid has finished writing the partials
     const int row = D + 2;
     const float* base = partials + (static_cast<int64_t>(s) * Hq + hq) * num_splits * row;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     // (m, l) of this warp's splits, folded per lane, then across the lanes
     float M = -INFINITY, L = 0.f;
     for (int sp = warp + nw * lane; sp < num_splits; sp += 32 * nw) {
@@ -644,11 +659,31 @@ cudaError_t launch_combine(const float* partials, float* out, int num_seqs, int 
                            int num_splits, cudaStream_t stream) {
     dim3 cgrid(static_cast<unsigned>(num_q_heads), static_cast<unsigned>(num_seqs));
     if (d > 256 || d % 2 != 0) return cudaErrorInvalidValue;
-    // about 8 splits per warp, at most kCombineMaxWarps warps
+    // about 8 splits per warp, at most kCombineMaxWarps warps; with one warp
+    // per (sequence, head), kCombineMaxWarps of them share a CTA
     int nw = (num_splits + 7) / 8;
     nw = nw < 1 ? 1 : (nw > kCombineMaxWarps ? kCombineMaxWarps : nw);
-    combine_kernel<<<cgrid, 32 * nw, 0, stream>>>(partials, out, num_q_heads, d, num_splits);
-    return cudaGetLastError();
+    // Launched with programmatic stream serialisation: its CTAs may become
+    // resident while the decode grid finishes, and wait for it on the device.
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.stream = stream;
+    cfg.dynamicSmemBytes = 0;
+    int one_warp = 0;
+    if (nw == 1) {
+        const long long pairs = static_cast<long long>(num_seqs) * num_q_heads;
+        cfg.gridDim = dim3(static_cast<unsigned>((pairs + kCombineMaxWarps - 1) / kCombineMaxWarps));
+        cfg.blockDim = dim3(32 * kCombineMaxWarps);
+        one_warp = 1;
+    } else {
+        cfg.gridDim = cgrid;
+        cfg.blockDim = dim3(32 * nw);
+    }
+    return cudaLaunchKernelEx(&cfg, combine_kernel, partials, out, num_seqs, num_q_heads, d, num_splits, one_warp);
 }
 
 // Resident CTAs per SM of the CUDA-core decode for these shapes.

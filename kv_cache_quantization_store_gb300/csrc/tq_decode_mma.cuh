@@ -463,6 +463,9 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     const int qstride = q_real ? Gq * 4 : 0;
     const uint2* qfrag2 = reinterpret_cast<const uint2*>(smem + G::q_off(Hq)) + warp * G::KSTEPS * 32 + lane;
 
+    // every CTA of the grid is resident: the merge kernel may be scheduled
+    grid_launch_dependents();
+
     // ---- per-thread constant offsets inside a stage.  Row k of the MMA tiles
     // holds token sig(k) of the chunk; the order is chosen on the host to
     // spread each warp's loads over the shared-memory banks. -------------------

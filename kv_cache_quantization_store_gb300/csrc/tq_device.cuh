@@ -140,6 +140,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
     return true;
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+// Programmatic dependent launch (sm_90+): a kernel lets the next kernel of
+// its stream, launched with programmatic stream serialisation, start
+// early; the dependent waits for this grid's completion (and its memory)
+// before reading what it wrote.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 // Makes mbarrier initialisations visible to the bulk-copy engine.
 __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
 // Shared-memory counter increment with acquire-release ordering; returns the old value.

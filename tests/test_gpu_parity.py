@@ -284,3 +284,34 @@ def test_key_distortion_matches_lloyd_max(cuda_device, bits, lloyd_max_mse):
     row = quality.measure(bits, 4, 128, "normal", 16384, cuda_device, nc_options=(False,))[0]
     assert row["key_rel_mse"] == pytest.approx(lloyd_max_mse, rel=0.05)
     assert row["value_cos"] > 0.99
+
+
+def test_decode_in_cuda_graph(cuda_device):
+    """The decode captured in a CUDA graph (its merge kernel is launched with
+    programmatic stream serialisation) replays to the eager result."""
+    wl = W.small("c4", [600, 31], layers=(2,))
+    layer_idx = wl.layers[-1]
+    k, v = wl.kv()
+    layer = oracle_layer(wl, layer_idx)
+    ocache, _ = oracle_cache(wl, layer, k, v)
+    cfg = host_cfg(wl)
+    cache = upload_cache(ocache, cfg, layer_idx, cuda_device)
+    q = bf16(wl.q(), cuda_device)
+    table = torch.from_numpy(wl.layout()[0]).to(cuda_device)
+    lens = torch.from_numpy(wl.seq_lens.astype(np.int32)).to(cuda_device)
+    max_len = int(wl.seq_lens.max())
+    for splits in (1, 4):
+        ws = torch.zeros(tq.tq_decode_workspace_size(cfg, 2, wl.num_q_heads, wl.num_kv_heads, wl.block_size, max_len,
+                                                     splits), dtype=torch.uint8, device=cuda_device)
+        eager = torch.empty((2, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=cuda_device)
+        tq.tq_decode_attention(cfg, q, cache, table, lens, max_len, eager, ws, num_splits=splits)
+        graphed = torch.full_like(eager, float("nan"))
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            tq.tq_decode_attention(cfg, q, cache, table, lens, max_len, graphed, ws, num_splits=splits)
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(graphed.cpu().numpy(), eager.cpu().numpy())
+    assert cache.error_flags() == 0
