@@ -175,3 +175,56 @@ def test_status_strings(libtq):
     assert [tq_status_str(i) for i in range(7)] == [
         "TQ_OK", "TQ_ERR_INVALID_ARG", "TQ_ERR_UNKNOWN_PRESET", "TQ_ERR_UNSUPPORTED", "TQ_ERR_WORKSPACE",
         "TQ_ERR_OUT_OF_RANGE", "TQ_ERR_CUDA"]
+
+
+def test_ring_argument_errors(libtq):
+    """tq_ring_append and tq_decode_attention_ring reject bad arguments
+    before anything is enqueued (status codes of tq_status)."""
+    from kv_cache_quantization_store_gb300 import tq_config_init
+
+    cfg = tq_config_init(64, 3, 4)
+
+    def append(k=64, v=64, n=1, cu=64, seqs=1, lens=64, rk=64, rv=64, r_len=128, cache=None, bt=64, mb=4, ws=64,
+               ws_bytes=1 << 10):
+        cache = cache or _cache()
+        return libtq.tq_ring_append(ctypes.byref(cfg), k, v, n, cu, seqs, lens, rk, rv, r_len, ctypes.byref(cache),
+                                    bt, mb, ws, ws_bytes, None)
+
+    assert append(seqs=0) == 0          # no sequences: nothing to do
+    assert append(r_len=0) == 3         # ring length outside [1, 128]
+    assert append(r_len=129) == 3
+    assert append(n=-1) == 1            # negative token count
+    assert append(mb=0) == 1            # no block-table columns
+    assert append(rk=None) == 1         # missing ring
+    assert append(k=None) == 1          # new tokens without rows
+    assert append(rk=72) == 1           # ring not 16-byte aligned
+    assert append(cu=66) == 1           # cu_new not 4-byte aligned
+    assert append(ws=None) == 4         # missing workspace
+    assert append(ws_bytes=8) == 4      # workspace too small
+    assert append(ws=72) == 4           # workspace not 16-byte aligned
+    assert libtq.tq_ring_workspace_size(-1) == 0
+    assert libtq.tq_ring_workspace_size(4) >= 5 * 8
+
+    def decode(r_len=128, rk=64, rv=64, hq=2, heads=1):
+        return libtq.tq_decode_attention_ring(ctypes.byref(cfg), 64, 1, hq, ctypes.byref(_cache(heads=heads)), 64, 4,
+                                              64, 64, 0.0, 0, rk, rv, r_len, 64, 64, 1 << 20, None)
+
+    assert decode(r_len=0) == 3
+    assert decode(r_len=200) == 3
+    assert decode(rk=None) == 1
+    assert decode(rv=72) == 1           # ring not 16-byte aligned
+    assert decode(hq=16) == 3           # GQA group above 8
+
+
+def test_ring_decode_workspace_has_one_more_partial(libtq):
+    """The ring decode's workspace holds the splits' partial states plus one
+    for the ring rows: S * Hq * (splits + 1) * (d + 2) fp32, in 256-byte units."""
+    from kv_cache_quantization_store_gb300 import tq_config_init
+
+    cfg = tq_config_init(64, 3, 4)
+    s, hq, h, splits = 2, 8, 4, 3
+    plain = libtq.tq_decode_workspace_size(ctypes.byref(cfg), s, hq, h, 16, 1000, splits)
+    ring = libtq.tq_decode_ring_workspace_size(ctypes.byref(cfg), s, hq, h, 16, 1000, splits)
+    up = lambda x: -(-x // 256) * 256
+    assert plain == up(s * hq * splits * 66 * 4)
+    assert ring == up(s * hq * (splits + 1) * 66 * 4)
