@@ -465,6 +465,9 @@ def measure_ring(tq, wl, cfg, cache, table, k_all, v_all, q, max_len, dev, strea
     def direct(i, st=stream):
         tq.tq_store_kv(cfg, k_steps[i], v_steps[i], slots_steps[i], cache, stream=st)
 
+    def one_kernel(i, st=stream):
+        tq.tq_ring_step(cfg, k_steps[i], v_steps[i], lens_steps[i], ring_k, ring_v, cache, table, stream=st)
+
     # per-call latency, host launch included (the device work of one step is small)
     refill()
     latency_ring = timed(append, r_len)
@@ -472,7 +475,7 @@ def measure_ring(tq, wl, cfg, cache, table, k_all, v_all, q, max_len, dev, strea
     # device time per step: the R steps of a cycle captured in one CUDA graph
     graphs = {}
     try:
-        for name, fn in (("ring", append), ("direct", direct)):
+        for name, fn in (("ring", append), ("step", one_kernel), ("direct", direct)):
             refill()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
@@ -485,7 +488,7 @@ def measure_ring(tq, wl, cfg, cache, table, k_all, v_all, q, max_len, dev, strea
         graph_error = str(exc).splitlines()[0]
     else:
         graph_error = None
-    per_step = {"ring": float("nan"), "direct": float("nan")}
+    per_step = {"ring": float("nan"), "step": float("nan"), "direct": float("nan")}
     for name, g in graphs.items():
         t = []
         for _ in range(cycles + 1):
@@ -516,8 +519,10 @@ def measure_ring(tq, wl, cfg, cache, table, k_all, v_all, q, max_len, dev, strea
                                                        stream=stream), 12)[2:]
     res = {"ring_tokens": r_len, "cycle_steps": r_len,
             "append_device_us_per_step": round(per_step["ring"], 2),
+            "ring_step_device_us_per_step": round(per_step["step"], 2),
             "store_direct_device_us_per_step": round(per_step["direct"], 2),
             "append_mtok_s": round(s_n / per_step["ring"], 2),
+            "ring_step_mtok_s": round(s_n / per_step["step"], 2),
             "store_direct_mtok_s": round(s_n / per_step["direct"], 2),
             "append_latency_us_median": round(statistics.median(latency_ring), 2),
             "store_direct_latency_us_median": round(statistics.median(latency_direct), 2),

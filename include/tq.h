@@ -270,6 +270,24 @@ TQ_API tq_status tq_ring_append(const tq_config* cfg, const void* k_dev, const v
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * tq_ring_step -- one decode step of ring-buffered sequences in a single
+ * kernel and without workspace: the same result as tq_ring_append with one
+ * new token per sequence (cu_new = 0, 1, ..., num_seqs).
+ *   k_dev, v_dev: bf16 [num_seqs, num_kv_heads, head_dim], row s the new
+ *                 token of sequence s (16-byte aligned)
+ *   seq_lens_dev: int32 [num_seqs], tokens of s before the step (negative:
+ *                 no token for s)
+ * The token completes a ring block when (seq_lens[s] + 1) mod R = 0: then
+ * ring rows 0 .. R-2 and the token are quantised into positions
+ * seq_lens[s] + 1 - R .. seq_lens[s]; otherwise the token is copied into
+ * ring row seq_lens[s] mod R.  Flags and ring arguments as tq_ring_append.
+ */
+TQ_API tq_status tq_ring_step(const tq_config* cfg, const void* k_dev, const void* v_dev, int32_t num_seqs,
+                              const int32_t* seq_lens_dev, void* ring_k_dev, void* ring_v_dev, int32_t ring_tokens,
+                              const tq_cache* cache, const int32_t* block_table_dev, int32_t max_blocks_per_seq,
+                              void* stream);
+
+/*
  * tq_decode_ring_workspace_size -- as tq_decode_workspace_size, for
  * tq_decode_attention_ring (one more partial state per query head).
  */

@@ -20,7 +20,8 @@ __all__ = [
     "TQError", "TqConfig", "TqCache", "PagedCache", "lib", "library_path",
     "tq_config_init", "tq_config_from_preset", "tq_layer_signs", "tq_store_kv",
     "tq_decode_workspace_size", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_dequant",
-    "tq_ring_workspace_size", "tq_ring_append", "tq_decode_ring_workspace_size", "tq_decode_attention_ring",
+    "tq_ring_workspace_size", "tq_ring_append", "tq_ring_step", "tq_decode_ring_workspace_size",
+    "tq_decode_attention_ring",
     "new_ring", "tq_status_str", "TQ_NOALLOC_SCRATCH_BYTES", "TQ_RING_TOKENS",
     "new_paged_cache", "tq_hybrid_page", "PRESETS",
 ]
@@ -118,6 +119,9 @@ _SIGNATURES = {
                                       ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(TqCache), ctypes.c_void_p,
                                       ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "tq_ring_step": (ctypes.c_int, [ctypes.POINTER(TqConfig), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                    ctypes.POINTER(TqCache), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     "tq_decode_ring_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(TqConfig), ctypes.c_int32, ctypes.c_int32,
                                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                         ctypes.c_int32]),
@@ -337,6 +341,25 @@ def tq_ring_append(cfg: TqConfig, k: torch.Tensor, v: torch.Tensor, cu_new: torc
         _dev(ring_k, torch.bfloat16, "ring_k"), _dev(ring_v, torch.bfloat16, "ring_v"), ring_k.shape[1],
         ctypes.byref(desc), _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def tq_ring_step(cfg: TqConfig, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor, ring_k: torch.Tensor,
+                 ring_v: torch.Tensor, cache: PagedCache, block_table: torch.Tensor, stream=None):
+    """One decode step, one new token per sequence: k, v bf16 [S, H, d];
+    seq_lens int32 [S], tokens before the step (tq_ring_step in include/tq.h)."""
+    num_seqs = seq_lens.shape[0]
+    if k.dim() != 3 or k.shape[0] != num_seqs or v.shape != k.shape:
+        raise ValueError("k and v must be [S, H, d] with one row per sequence")
+    if block_table.dim() != 2 or block_table.shape[0] != num_seqs:
+        raise ValueError("block_table must be [S, max_blocks]")
+    if ring_k.shape != ring_v.shape or ring_k.dim() != 4 or ring_k.shape[0] != num_seqs:
+        raise ValueError("ring_k and ring_v must be [S, R, H, d]")
+    desc = cache.descriptor()
+    _check(lib().tq_ring_step(
+        ctypes.byref(cfg), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"), num_seqs,
+        _dev(seq_lens, torch.int32, "seq_lens"), _dev(ring_k, torch.bfloat16, "ring_k"),
+        _dev(ring_v, torch.bfloat16, "ring_v"), ring_k.shape[1], ctypes.byref(desc),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1], _stream(stream)))
 
 
 def tq_decode_ring_workspace_size(cfg: TqConfig, num_seqs: int, num_q_heads: int, num_kv_heads: int,

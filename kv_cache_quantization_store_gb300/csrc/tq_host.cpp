@@ -391,6 +391,39 @@ tq_status tq_decode_attention_ring(const tq_config* cfg, const void* q_dev, int3
 
 size_t tq_ring_workspace_size(int32_t num_seqs) { return num_seqs < 0 ? 0 : tq::ring_workspace_bytes(num_seqs); }
 
+tq_status tq_ring_step(const tq_config* cfg, const void* k_dev, const void* v_dev, int32_t num_seqs,
+                       const int32_t* seq_lens_dev, void* ring_k_dev, void* ring_v_dev, int32_t ring_tokens,
+                       const tq_cache* cache, const int32_t* block_table_dev, int32_t max_blocks_per_seq,
+                       void* stream) {
+    if (cache == nullptr) return fail(TQ_ERR_INVALID_ARG, "cache is NULL");
+    tq::LayerParams lp;
+    tq_status st = layer_params(cfg, cache->layer_idx, &lp);
+    if (st != TQ_OK) return st;
+    tq::CacheGeom g;
+    st = cache_geom(cache, cfg, false, &g);
+    if (st != TQ_OK) return st;
+    if (num_seqs < 0 || max_blocks_per_seq <= 0) return fail(TQ_ERR_INVALID_ARG, "negative size argument");
+    if (ring_tokens < 1 || ring_tokens > TQ_RING_MAX_TOKENS)
+        return fail(TQ_ERR_UNSUPPORTED, "ring_tokens must be in [1, %d] (got %d)", TQ_RING_MAX_TOKENS, ring_tokens);
+    if (num_seqs == 0) return TQ_OK;
+    if (k_dev == nullptr || v_dev == nullptr || seq_lens_dev == nullptr || ring_k_dev == nullptr ||
+        ring_v_dev == nullptr || block_table_dev == nullptr)
+        return fail(TQ_ERR_INVALID_ARG, "k, v, seq_lens, rings and block_table must not be NULL");
+    if (!aligned(k_dev, 16) || !aligned(v_dev, 16) || !aligned(ring_k_dev, 16) || !aligned(ring_v_dev, 16))
+        return fail(TQ_ERR_INVALID_ARG, "k, v, ring_k and ring_v must be 16-byte aligned");
+    if (!aligned(seq_lens_dev, 4) || !aligned(block_table_dev, 4))
+        return fail(TQ_ERR_INVALID_ARG, "seq_lens and block_table must be 4-byte aligned");
+    int sms = 0;
+    st = sm_count(&sms);
+    if (st != TQ_OK) return st;
+    const cudaError_t e = tq::launch_ring_step(
+        lp, g, static_cast<const uint16_t*>(k_dev), static_cast<const uint16_t*>(v_dev), num_seqs, seq_lens_dev,
+        static_cast<uint16_t*>(ring_k_dev), static_cast<uint16_t*>(ring_v_dev), ring_tokens, block_table_dev,
+        max_blocks_per_seq, sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tq_ring_step launch");
+    return TQ_OK;
+}
+
 tq_status tq_ring_append(const tq_config* cfg, const void* k_dev, const void* v_dev, int64_t num_tokens,
                          const int32_t* cu_new_dev, int32_t num_seqs, const int32_t* seq_lens_dev, void* ring_k_dev,
                          void* ring_v_dev, int32_t ring_tokens, const tq_cache* cache,

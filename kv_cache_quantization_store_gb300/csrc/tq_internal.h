@@ -76,6 +76,12 @@ cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16
 // Ring-buffered store: packs every ring block the new tokens complete and
 // copies the rest into the ring (tq_store.cu).  workspace: ring_workspace_bytes.
 size_t ring_workspace_bytes(int num_seqs);
+// One new token per sequence (row s of k / v), one kernel: packs the ring
+// blocks the tokens complete and copies the other tokens into the ring.
+cudaError_t launch_ring_step(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
+                             int num_seqs, const int32_t* seq_lens, uint16_t* ring_k, uint16_t* ring_v,
+                             int ring_tokens, const int32_t* block_table, int max_blocks_per_seq, int sm_count,
+                             cudaStream_t stream);
 cudaError_t launch_ring_append(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
                                int64_t num_tokens, const int32_t* cu_new, int num_seqs, const int32_t* seq_lens,
                                uint16_t* ring_k, uint16_t* ring_v, int ring_tokens, const int32_t* block_table,

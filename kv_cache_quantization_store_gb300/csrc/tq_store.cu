@@ -81,16 +81,27 @@ __device__ __forceinline__ uint64_t pack8(const uint32_t* code) {
 // the call, N new ones); token t of the append list is position
 // R floor(L/R) + t - off[s] of the sequence with off[s] <= t < off[s + 1],
 // read from ring row p mod R (p < L) or from new row cu_new[s] + p - L.
+//
+// Step mode (one new token per sequence, row s of k / v): the list is the
+// fixed space of num_seqs x R ring rows.  Row i of sequence s is packed
+// when the new token completes its ring block ((L + 1) mod R = 0; row R - 1
+// is the new token itself); otherwise the new token is copied into ring row
+// L mod R.  A warp whose rows have neither job skips them.
 struct RingMap {
-    const int64_t* off;  // [num_seqs + 1]: exclusive scan of the packed counts
+    const int64_t* off;  // [num_seqs + 1]: exclusive scan of the packed counts (list mode)
     const int32_t* seq_lens;
     const int32_t* cu_new;
     const int32_t* block_table;
     const uint16_t* ring_k;
     const uint16_t* ring_v;
+    uint16_t* ring_k_w;  // step mode: the ring rows new tokens are copied into
+    uint16_t* ring_v_w;
     int num_seqs;
     int ring_tokens;
     int max_blocks;
+    int cap;    // tokens the block table can hold
+    int step;   // 1: step mode
+    int parts;  // step mode: CTAs sharing one sequence's ring block
 };
 
 // Validity and packed-token count of a sequence's append: L + N must fit the
@@ -139,8 +150,10 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     const int vin = lane / LPV;
     const int H = c.num_kv_heads;
     if constexpr (RING) {
-        const int64_t listed = rm.off[rm.num_seqs];  // num_tokens: the host's bound
-        num_tokens = listed < num_tokens ? listed : num_tokens;
+        if (!rm.step) {
+            const int64_t listed = rm.off[rm.num_seqs];  // num_tokens: the host's bound
+            num_tokens = listed < num_tokens ? listed : num_tokens;
+        }
     }
     const int64_t num_vecs = num_tokens * H;
 
@@ -180,23 +193,8 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
         bulk_copy(ring_sh + static_cast<uint32_t>(2 * sl + 1) * kSpan * 2, v + b * D, bytes, full_sh + 8u * sl);
     };
 
-    const int64_t step = static_cast<int64_t>(gridDim.x) * kStoreWarps * VPW;
-    int64_t base = (static_cast<int64_t>(blockIdx.x) * kStoreWarps + warp) * VPW;
-    if (kPrefetch && lane == 0 && base < num_vecs) issue(base, 0);
-    bool timed_out = false;
-    int it = 0;
-    for (; base < num_vecs; base += step, ++it) {
-        const int sl = it & 1;
-        if constexpr (kPrefetch) {
-            if (lane == 0 && base + step < num_vecs) {
-                fence_proxy_async();  // the other slot was read through the generic proxy
-                issue(base + step, sl ^ 1);
-            }
-            if (!mbar_wait(full_sh + 8u * sl, static_cast<uint32_t>((it >> 1) & 1))) {
-                timed_out = true;
-                break;
-            }
-        }
+    // ---- one warp step: the VPW vectors from `base` (staged in slot sl) --------
+    auto warp_step = [&](const int64_t base, const int sl) {
         const int64_t vi = base + vin;
         const bool valid = vi < num_vecs;
         const int64_t vsafe = valid ? vi : num_vecs - 1;
@@ -205,7 +203,36 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
         const uint16_t* krow = k + vsafe * D;
         const uint16_t* vrow = v + vsafe * D;
         int64_t slot_id = -1;
+        int64_t copy_row = -1;  // step mode: ring row the new token goes to
+        bool skip = false;      // step mode: neither job for this vector
         if constexpr (RING) {
+          if (rm.step) {
+            const int64_t t = vsafe / H;
+            const int h = static_cast<int>(vsafe - t * H);
+            const int R = rm.ring_tokens;
+            const int s_ = static_cast<int>(t / R);
+            const int i = static_cast<int>(t - static_cast<int64_t>(s_) * R);
+            const int L = rm.seq_lens[s_];
+            const bool ok = L >= 0 && L < rm.cap;
+            if (L >= rm.cap && valid && part == 0 && i == 0 && h == 0) set_flag(c.flags, kFlagSeq);
+            const int64_t new_row = static_cast<int64_t>(s_) * H + h;
+            if (ok && (L + 1) % R == 0) {
+                const int pos = L + 1 - R + i;
+                const int64_t r = (static_cast<int64_t>(s_) * R + i) * H + h;
+                krow = i < R - 1 ? rm.ring_k + r * D : k + new_row * D;
+                vrow = i < R - 1 ? rm.ring_v + r * D : v + new_row * D;
+                const int b = rm.block_table[static_cast<int64_t>(s_) * rm.max_blocks + pos / c.block_size];
+                if (b >= 0 && b < c.num_blocks) slot_id = static_cast<int64_t>(b) * c.block_size + pos % c.block_size;
+                else if (valid && part == 0) set_flag(c.flags, kFlagBlock);
+            } else if (ok && i == L % R) {
+                krow = k + new_row * D;
+                vrow = v + new_row * D;
+                copy_row = (static_cast<int64_t>(s_) * R + i) * H + h;
+            } else {
+                skip = true;
+            }
+            skip = skip || !valid;
+          } else {
             const int64_t t = vsafe / H;
             const int h = static_cast<int>(vsafe - t * H);
             int lo = 0, hi = rm.num_seqs;  // off[lo] <= t < off[hi]
@@ -230,6 +257,7 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
             const int b = rm.block_table[static_cast<int64_t>(s_) * rm.max_blocks + pos / c.block_size];
             if (b >= 0 && b < c.num_blocks) slot_id = static_cast<int64_t>(b) * c.block_size + pos % c.block_size;
             else if (valid && part == 0 && h == 0) set_flag(c.flags, kFlagBlock);
+          }
         } else {
             if (valid) slot_id = slot_mapping[vsafe / H];
         }
@@ -240,6 +268,21 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                                       : reinterpret_cast<const uint4*>(vrow) + part;
         // 16-byte group j of K or V: shared memory (staged) or read-only global
         auto ld16 = [&](const uint4* src, int j) -> uint4 { return kPrefetch ? src[LPV * j] : __ldg(src + LPV * j); };
+        if constexpr (RING) {
+            if (rm.step) {
+                if (copy_row >= 0 && valid) {
+                    uint4* kd = reinterpret_cast<uint4*>(rm.ring_k_w + copy_row * D) + part;
+                    uint4* vd = reinterpret_cast<uint4*>(rm.ring_v_w + copy_row * D) + part;
+#pragma unroll
+                    for (int j = 0; j < EPL / 8; ++j) {
+                        kd[LPV * j] = ksrc[LPV * j];
+                        vd[LPV * j] = vsrc[LPV * j];
+                    }
+                }
+                // nothing to pack in this warp step (the copies are done)
+                if (!__any_sync(kFull, !skip && copy_row < 0)) return;
+            }
+        }
 
         // ---- key -----------------------------------------------------------
         {
@@ -385,6 +428,60 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                 reinterpret_cast<uint16_t*>(d)[u - vv * kPerSlot] = reinterpret_cast<const uint16_t*>(stage)[u];
         }
         __syncwarp();
+    };
+
+    if constexpr (RING) {
+        if (rm.step) {
+            // Step mode: `parts` CTAs per sequence.  They pack the ring block
+            // the new token completes (R x H vectors, interleaved by warp
+            // step), or the first copies the token into its ring row.
+            const int R = rm.ring_tokens;
+            const int parts = rm.parts;
+            const int64_t per_seq = static_cast<int64_t>(R) * H;
+            for (int idx = blockIdx.x; idx < rm.num_seqs * parts; idx += gridDim.x) {
+                const int s_ = idx / parts, part_ = idx - s_ * parts;
+                const int L = rm.seq_lens[s_];
+                if (L >= rm.cap && threadIdx.x == 0 && part_ == 0) set_flag(c.flags, kFlagSeq);
+                if (L < 0 || L >= rm.cap) continue;
+                if ((L + 1) % R == 0) {
+                    for (int64_t b0 = s_ * per_seq + (static_cast<int64_t>(part_) * kStoreWarps + warp) * VPW;
+                         b0 < (s_ + 1) * per_seq; b0 += static_cast<int64_t>(parts) * kStoreWarps * VPW)
+                        warp_step(b0, 0);
+                } else if (part_ == 0) {
+                    const int units = H * D / 8;  // 16-byte units of the token's H rows
+                    const uint4* ks = reinterpret_cast<const uint4*>(k + static_cast<int64_t>(s_) * H * D);
+                    const uint4* vs = reinterpret_cast<const uint4*>(v + static_cast<int64_t>(s_) * H * D);
+                    const int64_t row = (static_cast<int64_t>(s_) * R + L % R) * H * D;
+                    uint4* kd = reinterpret_cast<uint4*>(rm.ring_k_w + row);
+                    uint4* vd = reinterpret_cast<uint4*>(rm.ring_v_w + row);
+                    for (int u = threadIdx.x; u < units; u += blockDim.x) {
+                        kd[u] = __ldg(ks + u);
+                        vd[u] = __ldg(vs + u);
+                    }
+                }
+            }
+            return;
+        }
+    }
+
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kStoreWarps * VPW;
+    int64_t base = (static_cast<int64_t>(blockIdx.x) * kStoreWarps + warp) * VPW;
+    if (kPrefetch && lane == 0 && base < num_vecs) issue(base, 0);
+    bool timed_out = false;
+    int it = 0;
+    for (; base < num_vecs; base += step, ++it) {
+        const int sl = it & 1;
+        if constexpr (kPrefetch) {
+            if (lane == 0 && base + step < num_vecs) {
+                fence_proxy_async();  // the other slot was read through the generic proxy
+                issue(base + step, sl ^ 1);
+            }
+            if (!mbar_wait(full_sh + 8u * sl, static_cast<uint32_t>((it >> 1) & 1))) {
+                timed_out = true;
+                break;
+            }
+        }
+        warp_step(base, sl);
     }
     if (timed_out) {
         if (lane == 0) {
@@ -406,7 +503,20 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const uint16_t* k, 
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     const int grid = static_cast<int>(want < cap ? want : cap);
     if (rm != nullptr) {
-        store_kernel<D, KB, VB, true><<<grid, kStoreWarps * 32, 0, stream>>>(p, c, k, v, num_tokens, nullptr, *rm);
+        RingMap r = *rm;
+        int g = grid;
+        if (r.step) {
+            // step mode: enough CTAs per sequence that a block completed by
+            // few sequences still spreads over about one CTA per SM
+            const int per_seq_steps = (r.ring_tokens * c.num_kv_heads + VPW - 1) / VPW;
+            const int max_parts = (per_seq_steps + kStoreWarps - 1) / kStoreWarps;
+            int parts = (sm_count + r.num_seqs - 1) / r.num_seqs;
+            parts = parts < 1 ? 1 : (parts > max_parts ? max_parts : parts);
+            r.parts = parts;
+            const int64_t want_step = static_cast<int64_t>(r.num_seqs) * parts;
+            g = static_cast<int>(want_step < cap ? want_step : cap);
+        }
+        store_kernel<D, KB, VB, true><<<g, kStoreWarps * 32, 0, stream>>>(p, c, k, v, num_tokens, nullptr, r);
         return cudaGetLastError();
     }
     const int ring_bytes = KB != 8 ? kStoreWarps * 4 * VPW * D * 2 : 0;
@@ -539,6 +649,16 @@ cudaError_t launch_store(const LayerParams& p, const CacheGeom& c, const uint16_
     return dispatch_d(p, c, k, v, num_tokens, slot_mapping, nullptr, sm_count, stream);
 }
 
+cudaError_t launch_ring_step(const LayerParams& p, const CacheGeom& c, const uint16_t* k, const uint16_t* v,
+                             int num_seqs, const int32_t* seq_lens, uint16_t* ring_k, uint16_t* ring_v,
+                             int ring_tokens, const int32_t* block_table, int max_blocks_per_seq, int sm_count,
+                             cudaStream_t stream) {
+    if (num_seqs <= 0) return cudaSuccess;
+    RingMap rm{nullptr, seq_lens, nullptr, block_table, ring_k, ring_v, ring_k, ring_v, num_seqs, ring_tokens,
+               max_blocks_per_seq, max_blocks_per_seq * c.block_size, 1, 1};
+    return dispatch_d(p, c, k, v, static_cast<int64_t>(num_seqs) * ring_tokens, nullptr, &rm, sm_count, stream);
+}
+
 size_t ring_workspace_bytes(int num_seqs) {
     return (static_cast<size_t>(num_seqs > 0 ? num_seqs : 0) + 1) * sizeof(int64_t) + 256;
 }
@@ -556,7 +676,8 @@ cudaError_t launch_ring_append(const LayerParams& p, const CacheGeom& c, const u
     if (e != cudaSuccess) return e;
     // every packed position is an old ring row or a new token: at most
     // num_tokens + num_seqs (R - 1) of them
-    RingMap rm{off, seq_lens, cu_new, block_table, ring_k, ring_v, num_seqs, ring_tokens, max_blocks_per_seq};
+    RingMap rm{off, seq_lens, cu_new, block_table, ring_k, ring_v, ring_k, ring_v, num_seqs, ring_tokens,
+               max_blocks_per_seq, cap, 0, 1};
     const int64_t bound = num_tokens + static_cast<int64_t>(num_seqs) * (ring_tokens - 1);
     e = dispatch_d(p, c, k, v, bound, nullptr, &rm, sm_count, stream);
     if (e != cudaSuccess) return e;

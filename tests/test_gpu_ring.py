@@ -37,8 +37,9 @@ CASES = ring_cases()
 IDS = [w.name for w in CASES]
 
 
-def run_appends(wl, r_len, device):
-    """The same prefill and decode steps on the GPU and in the oracle.
+def run_appends(wl, r_len, device, api="append"):
+    """The same prefill and decode steps on the GPU and in the oracle; the
+    GPU's decode steps go through tq_ring_append or tq_ring_step (api).
     Returns (gpu cache, gpu rings, oracle cache, oracle rings, near dict, cfg, layer)."""
     layer = oracle_layer(wl, 0)
     cfg = host_cfg(wl)
@@ -66,19 +67,29 @@ def run_appends(wl, r_len, device):
         tq.tq_ring_append(cfg, kt, vt, torch.from_numpy(cu_new).to(device),
                           torch.tensor(lens, dtype=torch.int32, device=device), grk, grv, gcache, gtable, ws)
 
+    def step(rows, lens):
+        """One token per sequence through tq_ring_step (idle sequences: seq_lens -1, any row)."""
+        cu_new = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+        idx = np.concatenate([np.asarray(r, dtype=np.int64) for r in rows])
+        near.update(O.ring_append(layer, ocache, table, ork, orv, np.asarray(lens), k_all[idx], v_all[idx], cu_new))
+        one = np.array([r[0] if r else 0 for r in rows], dtype=np.int64)
+        tq.tq_ring_step(cfg, bf16(k_all[one], device), bf16(v_all[one], device),
+                        torch.tensor(lens, dtype=torch.int32, device=device), grk, grv, gcache, gtable)
+
     both([range(cu[s], cu[s] + PROMPTS[s]) for s in range(n_seq)], [0] * n_seq)
     for i in range(max(STEPS)):
         rows = [[cu[s] + PROMPTS[s] + i] if i < STEPS[s] else [] for s in range(n_seq)]
         lens = [PROMPTS[s] + i if i < STEPS[s] else -1 for s in range(n_seq)]
-        both(rows, lens)
+        (step if api == "step" else both)(rows, lens)
     torch.cuda.synchronize()
     return gcache, (grk, grv), ocache, (ork, orv), near, cfg, layer
 
 
+@pytest.mark.parametrize("api", ["append", "step"])
 @pytest.mark.parametrize("r_len", [32, 128])
 @pytest.mark.parametrize("wl", CASES, ids=IDS)
-def test_ring_append_parity(cuda_device, wl, r_len):
-    gcache, (grk, grv), ocache, (ork, orv), near, cfg, layer = run_appends(wl, r_len, cuda_device)
+def test_ring_append_parity(cuda_device, wl, r_len, api):
+    gcache, (grk, grv), ocache, (ork, orv), near, cfg, layer = run_appends(wl, r_len, cuda_device, api)
     assert gcache.error_flags() == 0
     k_all, _ = wl.kv()
     cu = wl.cu_seqlens()

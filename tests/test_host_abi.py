@@ -205,6 +205,17 @@ def test_ring_argument_errors(libtq):
     assert libtq.tq_ring_workspace_size(-1) == 0
     assert libtq.tq_ring_workspace_size(4) >= 5 * 8
 
+    def step(k=64, v=64, seqs=1, lens=64, rk=64, rv=64, r_len=128, bt=64, mb=4):
+        return libtq.tq_ring_step(ctypes.byref(cfg), k, v, seqs, lens, rk, rv, r_len, ctypes.byref(_cache()), bt, mb,
+                                  None)
+
+    assert step(seqs=0) == 0
+    assert step(r_len=0) == 3
+    assert step(seqs=-1) == 1
+    assert step(k=None) == 1
+    assert step(rv=80 + 8) == 1         # ring not 16-byte aligned
+    assert step(lens=66) == 1           # seq_lens not 4-byte aligned
+
     def decode(r_len=128, rk=64, rv=64, hq=2, heads=1):
         return libtq.tq_decode_attention_ring(ctypes.byref(cfg), 64, 1, hq, ctypes.byref(_cache(heads=heads)), 64, 4,
                                               64, 64, 0.0, 0, rk, rv, r_len, 64, 64, 1 << 20, None)
