@@ -144,12 +144,19 @@ def measured_peaks():
 
 
 def decode_source_digest() -> str:
-    """sha256 (16 hex digits) over the decode kernel sources, in name order."""
+    """sha256 (16 hex digits) over the code of the decode kernel sources, in
+    name order: comments are dropped and whitespace runs collapsed, so that
+    editing a comment does not void a traffic record of unchanged code."""
+    import re
+
     csrc = ROOT / "kv_cache_quantization_store_gb300" / "csrc"
     h = hashlib.sha256()
     for f in sorted(csrc.glob("tq_decode*")):
+        text = f.read_text()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
         h.update(f.name.encode())
-        h.update(f.read_bytes())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

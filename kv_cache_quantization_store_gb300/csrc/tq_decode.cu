@@ -1,20 +1,26 @@
-// Fused decode attention over the packed cache, split-KV.
+// Decode host entry (launch_decode) and the kernels around the
+// tensor-core decode of tq_decode_mma.cuh:
+//   - the CUDA-core decode for the shapes the tensor-core path does not
+//     take (d < 64, other KV-head counts, G > 8);
+//   - the split planner;
+//   - the log-sum-exp merge of the split partials;
+//   - the ring rows' partial state and the side stream it runs on.
 //
 // [ART] hnwysp.cn TurboQuant article, "Direction 1": score the rotated query
 // against the compressed keys (q . k_hat = vec_norm * (Pi q) . c~), run an
 // online softmax block by block, never expand K or V.  [TQC] norm_correction
 // divides by ||c~|| (the centroid vector's norm).
 //
-// Grid: (split, sequence).  A CTA walks its range of 16-token chunks; each
-// chunk is the contiguous span of 16 token rows (all KV heads) inside one
-// paged block, staged into shared memory with 16-byte cp.async copies
-// (double-buffered).  Per chunk:
+// CUDA-core decode.  Grid: (split, sequence).  A CTA walks its range of
+// 16-token chunks; each chunk is the contiguous span of 16 token rows (all
+// KV heads) inside one paged block, staged into shared memory with 16-byte
+// cp.async copies (double-buffered).  Per chunk:
 //   1. scores: (token, head) items, a few threads each, dot the rotated,
 //      pre-scaled queries with the looked-up centroids (or FP8 keys);
 //   2. online-softmax update per query head (max, rescale, probabilities);
 //   3. P.V: warp h owns KV head h, each lane d/32 dims of all its queries.
-// Each CTA writes a partial (m, l, o) per query head; a second kernel merges
-// the splits by log-sum-exp.
+// Each CTA writes a partial (m, l, o) per query head; the merge kernel
+// combines the splits by log-sum-exp.
 #include <cmath>
 
 #include <mutex>

@@ -11,36 +11,45 @@
 // Work decomposition.  A CTA owns one sequence's split (a range of 16-token
 // chunks) and has WPH warps per KV head (H heads, compile-time).  Each chunk
 // -- 16 consecutive tokens of every head, contiguous and 16-byte aligned in a
-// paged block -- is staged into shared memory with 16-byte cp.async copies
-// through an NS-deep ring whose stage slots and per-thread offsets are
-// compile-time constants.  The WPH warps of a head split its dims: each
+// paged block -- is staged into shared memory by one bulk copy
+// (cp.async.bulk) that completes the stage's mbarrier, through an NS-deep
+// ring whose stage slots and per-thread offsets are compile-time constants.
+// A warp releases a stage once its data is in registers; the last warp to
+// release it refills it.  The WPH warps of a head split its dims: each
 // computes a partial QK over its share, the partials are added through
 // shared memory, and each computes P.V for its share of the output.
 //
-//   QK   S[16 tok x 8 q] = Khat[16 x d] * Q'^T[d x 8]
+// Prologue: the first chunks are in flight while the query rotation runs
+// in the ring's last stages (one warp per query row: shuffles and register
+// butterflies), then the pair table and the query fragments are built.
+//
+//   QK   S[16 tok x 8 cols] = Khat[16 x d] * Q'^T[d x 8]
 //        Thread (r = lane/4, c = lane%4) feeds key dims of tokens r and
 //        r+8; each A register is one pair of consecutive dims, looked up
-//        from a per-lane-replicated pair table in shared memory (3-bit: 64
-//        entries of {half2 c, float c0^2+c1^2}; 4-bit: 256 entries of half2
-//        c), or converted from two FP8 bytes.  Q' is permuted to the same dim
-//        order and split into fp16 hi + lo parts (two MMAs), and the table
-//        holds the centroids times a scale chosen so that their fp16 rounding
-//        error is small; together they keep the scores near fp32 accuracy.
-//   norm 3-bit: the table's squared sums; 4-bit: Khat*Khat (HMUL2) against a
-//        ones column, one extra MMA per k-step.
+//        from a per-lane-replicated pair table of half2 centroids in shared
+//        memory (3-bit: 64 entries, 4-bit: 256), or converted from two FP8
+//        bytes.  Q' is permuted to the same dim order and split into fp16 hi
+//        + lo parts: with G <= 4 columns 0-3 carry the hi and 4-7 the lo
+//        parts (one MMA and a shuffle), else two MMAs.  The table holds the
+//        centroids times a scale chosen so that their fp16 rounding error is
+//        small; together this keeps the scores near fp32 accuracy.
+//   norm (norm correction) Khat*Khat (HMUL2) against a ones column, one
+//        extra MMA per k-step.
 //   softmax  per query column, lazily rescaled (only when the running max
 //        grows by more than 2^8).
 //   PV   O^T[d x 8 q] += V^T[d x 16 tok] * P'[16 tok x 8 q], P' = p * scale_t.
 //        Thread r feeds value dims of tokens 2c, 2c+1, 2c+8, 2c+9 as fp16
-//        1 + code / 2^VB (bit placement, no conversion); an extra M-tile
-//        whose row 0 is all ones accumulates sum P', which removes the +1
-//        exactly and re-centres the codes on the middle of their range.  P
-//        moves into the B layout with movmatrix.  The zero points enter as
-//        sum p * (zero_t + centre * scale_t) in fp32.
+//        subnormals code * 2^(pos - 24), masked in place from their bytes; a
+//        per-dim power of two restores them at the end.  An extra M-tile whose
+//        row 0 is all ones accumulates sum P', which re-centres the codes on
+//        the middle of their range.  P moves into the B layout with
+//        movmatrix.  The zero points enter as sum p * (zero_t + centre *
+//        scale_t) in fp32.
 //
 // Each warp writes its dims of a partial (m, l, o) per query head; the
-// combine kernel merges the splits by log-sum-exp.  Every call writes every
-// partial it reads, so the workspace needs no clearing between calls.
+// merge kernel (tq_decode.cu) combines the splits by log-sum-exp and waits
+// for this grid through programmatic dependent launch.  Every call writes
+// every partial it reads, so the workspace needs no clearing between calls.
 #pragma once
 
 #include <atomic>
