@@ -201,6 +201,14 @@ class ClockSampler:
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        if self.proc is not None:
+            # the timed region starts once samples are flowing (at most 3 s)
+            import time
+            t0 = time.monotonic()
+            while time.monotonic() - t0 < 3.0 and self.proc.poll() is None:
+                if Path(self.file.name).stat().st_size > 0:
+                    break
+                time.sleep(0.02)
         return self
 
     def __exit__(self, *exc):
