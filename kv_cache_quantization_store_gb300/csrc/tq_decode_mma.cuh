@@ -739,7 +739,21 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 #pragma unroll
         for (int mt = 0; mt < G::MTILES; ++mt) {
             uint32_t vf[4];
-            if constexpr (G::VUNITS) {
+            if constexpr (G::VUNITS && G::VUNIT == 2) {
+                // local dims 2mt, 2mt + 1 share byte b of unit m.  The units
+                // are zero-extended 16-bit loads, so one PRMT gives both
+                // tokens' byte b with a zero byte above it: the odd dim enters
+                // as the whole byte (16 hi + lo) and the epilogue subtracts
+                // the even dim's sum (lo), which the same MMA produces.
+                const int m = (2 * mt) / G::VDPU, b = ((2 * mt) % G::VDPU) / 2;
+                const uint32_t sel = b | (2 << 4) | ((b + 4) << 8) | (6 << 12);
+                const uint32_t win0 = prmt(vr.w0[m], vr.w1[m], sel);
+                const uint32_t win8 = prmt(vr.w8[m], vr.w9[m], sel);
+                vf[0] = win0 & 0x000F000Fu;
+                vf[1] = win0;
+                vf[2] = win8 & 0x000F000Fu;
+                vf[3] = win8;
+            } else if constexpr (G::VUNITS) {
                 // local dims 2mt, 2mt + 1 share one byte of unit m
                 const int m = (2 * mt) / G::VDPU, w = (2 * mt) % G::VDPU;
                 vf[0] = value_unit_sub(vr.w0[m], vr.w1[m], w);
@@ -885,8 +899,10 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
                 w0 = value_weight<VB>(2 * mt);
                 w1 = value_weight<VB>(2 * mt + 1);
             }
+            // (2-byte value units: row r + 8 holds 16 hi + lo, row r holds lo)
+            const float odd = (G::VUNITS && G::VUNIT == 2) ? o[mt][2 + e] - o[mt][e] : o[mt][2 + e];
             part_out[2 + d0] = fmaf(o[mt][e], w0, -cb) + z;
-            part_out[2 + d0 + 1] = fmaf(o[mt][2 + e], w1, -cb) + z;
+            part_out[2 + d0 + 1] = fmaf(odd, w1, -cb) + z;
         }
     }
 }
