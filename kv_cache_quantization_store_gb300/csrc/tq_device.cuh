@@ -100,6 +100,27 @@ __device__ __forceinline__ float half_from_bits(uint32_t b) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
 }
 
+// Unsigned 32-bit division by an invariant divisor d >= 1 with one
+// multiply-high (T. Granlund and P. Montgomery, "Division by invariant
+// integers using multiplication", PLDI 1994, the round-up method):
+// l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, and
+// n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0) with t = mulhi(m, n).
+struct FastDiv {
+    uint32_t m, s1, s2;
+};
+
+inline FastDiv make_fast_div(uint32_t d) {
+    uint32_t l = 0;
+    while (l < 32 && (1ull << l) < d) ++l;
+    const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+    return FastDiv{static_cast<uint32_t>(m), l < 1 ? l : 1u, l > 1 ? l - 1 : 0u};
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& d) {
+    const uint32_t t = __umulhi(d.m, n);
+    return (t + ((n - t) >> d.s1)) >> d.s2;
+}
+
 __device__ __forceinline__ void set_flag(uint32_t* flags, uint32_t bit) {
     if (flags != nullptr) atomicOr(flags, bit);
 }

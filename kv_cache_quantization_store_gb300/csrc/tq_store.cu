@@ -115,7 +115,8 @@ template <int D, int KB, int VB, bool RING>
 __global__ void __launch_bounds__(kStoreWarps * 32)
 store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict__ k,
              const uint16_t* __restrict__ v, int64_t num_tokens,
-             const int64_t* __restrict__ slot_mapping, const RingMap rm) {
+             const int64_t* __restrict__ slot_mapping, const RingMap rm, const FastDiv div_h,
+             const FastDiv div_bs, const int narrow) {
     using S = Slot<D, KB, VB>;
     using LS = LaneSplit<D>;
     constexpr int EPL = LS::kEPL, LPV = LS::kLPV, VPW = LS::kVPW;
@@ -259,7 +260,12 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
             else if (valid && part == 0 && h == 0) set_flag(c.flags, kFlagBlock);
           }
         } else {
-            if (valid) slot_id = slot_mapping[vsafe / H];
+            if (valid) {
+                // narrow: every vector index fits 32 bits (host-checked)
+                const int64_t t = narrow ? static_cast<int64_t>(fast_div(static_cast<uint32_t>(vsafe), div_h))
+                                         : vsafe / H;
+                slot_id = slot_mapping[t];
+            }
         }
         // this lane's groups: 16 bytes at element 8 (part + LPV j) of its vector
         const uint4* ksrc = kPrefetch ? reinterpret_cast<const uint4*>(ring + 2 * sl * kSpan + vin * D) + part
@@ -406,11 +412,13 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
         // ---- scatter the warp's slots ---------------------------------------
         uint64_t dst = 0;
         if (valid && part == 0) {
-            const int64_t t = vi / H;
+            const int64_t t = narrow ? static_cast<int64_t>(fast_div(static_cast<uint32_t>(vi), div_h)) : vi / H;
             const int h = static_cast<int>(vi - t * H);
             const int64_t slot = slot_id;
             if (slot >= 0) {
-                const int64_t blk = slot / c.block_size;
+                const int64_t blk = narrow && slot < (int64_t{1} << 32)
+                                        ? static_cast<int64_t>(fast_div(static_cast<uint32_t>(slot), div_bs))
+                                        : slot / c.block_size;
                 const int64_t pos = slot - blk * c.block_size;
                 if (blk < c.num_blocks)
                     dst = reinterpret_cast<uint64_t>(c.data + blk * c.block_stride + (pos * H + h) * SA);
@@ -502,6 +510,9 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const uint16_t* k, 
     const int64_t want = (warps + kStoreWarps - 1) / kStoreWarps;
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     const int grid = static_cast<int>(want < cap ? want : cap);
+    const FastDiv div_h = make_fast_div(static_cast<uint32_t>(c.num_kv_heads));
+    const FastDiv div_bs = make_fast_div(static_cast<uint32_t>(c.block_size));
+    const int narrow = vecs < (int64_t{1} << 32) ? 1 : 0;
     if (rm != nullptr) {
         RingMap r = *rm;
         int g = grid;
@@ -516,14 +527,16 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const uint16_t* k, 
             const int64_t want_step = static_cast<int64_t>(r.num_seqs) * parts;
             g = static_cast<int>(want_step < cap ? want_step : cap);
         }
-        store_kernel<D, KB, VB, true><<<g, kStoreWarps * 32, 0, stream>>>(p, c, k, v, num_tokens, nullptr, r);
+        store_kernel<D, KB, VB, true><<<g, kStoreWarps * 32, 0, stream>>>(p, c, k, v, num_tokens, nullptr, r, div_h,
+                                                                          div_bs, narrow);
         return cudaGetLastError();
     }
     const int ring_bytes = KB != 8 ? kStoreWarps * 4 * VPW * D * 2 : 0;
     auto kern = store_kernel<D, KB, VB, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ring_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kStoreWarps * 32, ring_bytes, stream>>>(p, c, k, v, num_tokens, slot_mapping, RingMap{});
+    kern<<<grid, kStoreWarps * 32, ring_bytes, stream>>>(p, c, k, v, num_tokens, slot_mapping, RingMap{}, div_h,
+                                                         div_bs, narrow);
     return cudaGetLastError();
 }
 
