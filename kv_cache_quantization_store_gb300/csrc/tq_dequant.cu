@@ -43,7 +43,8 @@ template <int D, int KB, int VB>
 __global__ void __launch_bounds__(kDqWarps * 32)
 dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict__ block_table,
                const int max_blocks, const int32_t* __restrict__ cu_seqlens, const int max_seq_len,
-               uint16_t* __restrict__ k_out, uint16_t* __restrict__ v_out) {
+               uint16_t* __restrict__ k_out, uint16_t* __restrict__ v_out, const FastDiv div_h,
+               const FastDiv div_bs, const int narrow) {
     using S = Slot<D, KB, VB>;
     using LS = LaneSplit<D>;
     constexpr int EPL = LS::kEPL, LPV = LS::kLPV, VPW = LS::kVPW;
@@ -84,13 +85,17 @@ dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict
          base += step) {
         const int64_t vi = base + vin;
         const bool valid = vi < num_vecs;
-        const int pos = valid ? static_cast<int>(vi / H) : 0;
+        // narrow: vector indices fit 32 bits (host-checked); positions always do
+        const int pos = valid ? (narrow ? static_cast<int>(fast_div(static_cast<uint32_t>(vi), div_h))
+                                        : static_cast<int>(vi / H))
+                              : 0;
         const int h = valid ? static_cast<int>(vi - static_cast<int64_t>(pos) * H) : 0;
-        const int blk = valid ? block_table[static_cast<int64_t>(s) * max_blocks + pos / c.block_size] : 0;
+        const int col = static_cast<int>(fast_div(static_cast<uint32_t>(pos), div_bs));  // pos / block_size
+        const int blk = valid ? block_table[static_cast<int64_t>(s) * max_blocks + col] : 0;
         const bool ok = valid && blk >= 0 && blk < c.num_blocks;
         if (valid && !ok && part == 0) set_flag(c.flags, kFlagBlock);
         const uint8_t* slot = c.data + static_cast<int64_t>(ok ? blk : 0) * c.block_stride +
-                              (static_cast<int64_t>(pos % c.block_size) * H + h) * SA;
+                              (static_cast<int64_t>(pos - col * c.block_size) * H + h) * SA;
         uint4* kdst = reinterpret_cast<uint4*>(k_out + ((row0 + pos) * H + h) * D) + part;
         uint4* vdst = reinterpret_cast<uint4*>(v_out + ((row0 + pos) * H + h) * D) + part;
 
@@ -167,8 +172,11 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const int32_t* bt, 
     if (gx > 1024) gx = 1024;
     if (gx < 1) gx = 1;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(num_seqs));
+    const FastDiv div_h = make_fast_div(static_cast<uint32_t>(c.num_kv_heads));
+    const FastDiv div_bs = make_fast_div(static_cast<uint32_t>(c.block_size));
+    const int narrow = vecs < (int64_t{1} << 32) ? 1 : 0;
     dequant_kernel<D, KB, VB><<<grid, kDqWarps * 32, 0, stream>>>(p, c, bt, max_blocks, cu, max_seq_len,
-                                                                   k_out, v_out);
+                                                                   k_out, v_out, div_h, div_bs, narrow);
     return cudaGetLastError();
 }
 
