@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kStoreWarps * 32)
 store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict__ k,
              const uint16_t* __restrict__ v, int64_t num_tokens,
              const int64_t* __restrict__ slot_mapping, const RingMap rm, const FastDiv div_h,
-             const FastDiv div_bs, const int narrow) {
+             const FastDiv div_bs, const int narrow, const int row_unit) {
     using S = Slot<D, KB, VB>;
     using LS = LaneSplit<D>;
     constexpr int EPL = LS::kEPL, LPV = LS::kLPV, VPW = LS::kVPW;
@@ -136,7 +136,8 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     // 0-2 and the bits above the lane bits, and the shuffle stages the lane
     // bits.  Each 8-element group is 16 contiguous bf16 bytes (the 8 lanes of
     // a quarter-warp read 128 contiguous bytes) and packs to whole bytes.
-    __shared__ __align__(16) uint8_t stage_all[kStoreWarps][VPW * SA + 2];
+    // (rows padded to 16 bytes, so that every warp's stage is 16-byte aligned)
+    __shared__ __align__(16) uint8_t stage_all[kStoreWarps][(VPW * SA + 2 + 15) / 16 * 16];
     // per lane part: XOR masks that flip the sign bits of the bf16 pairs the
     // random signs negate, word w of group j at [4 j + w]
     __shared__ __align__(16) uint32_t sign_mask[LPV][EPL / 2];
@@ -426,14 +427,39 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                     set_flag(c.flags, kFlagSlot);
             }
         }
-        constexpr int kUnits = VPW * SA / 2;
-        constexpr int kPerSlot = SA / 2;
+        if (row_unit != 0) {
+            // The warp step covers whole tokens (VPW a multiple of H): a
+            // token's H slots are one contiguous row of the cache, copied in
+            // row_unit-byte units (the host checked the alignment of the
+            // rows, the cache and the block stride).
+            const int rows = VPW / H;
+            const int row_bytes = H * SA;
 #pragma unroll 1
-        for (int u = lane; u < (kUnits + 31) / 32 * 32; u += 32) {
-            const int vv = min(u / kPerSlot, VPW - 1);
-            const uint64_t d = __shfl_sync(kFull, dst, vv * LPV);
-            if (u < kUnits && d != 0)
-                reinterpret_cast<uint16_t*>(d)[u - vv * kPerSlot] = reinterpret_cast<const uint16_t*>(stage)[u];
+            for (int tl = 0; tl < rows; ++tl) {
+                const uint64_t d = __shfl_sync(kFull, dst, tl * H * LPV);  // head 0 of token tl
+                if (d == 0) continue;
+                const uint8_t* src = stage + tl * row_bytes;
+                if (row_unit == 16) {
+                    for (int u = lane; u < row_bytes / 16; u += 32)
+                        reinterpret_cast<uint4*>(d)[u] = reinterpret_cast<const uint4*>(src)[u];
+                } else if (row_unit == 8) {
+                    for (int u = lane; u < row_bytes / 8; u += 32)
+                        reinterpret_cast<uint2*>(d)[u] = reinterpret_cast<const uint2*>(src)[u];
+                } else {
+                    for (int u = lane; u < row_bytes / 4; u += 32)
+                        reinterpret_cast<uint32_t*>(d)[u] = reinterpret_cast<const uint32_t*>(src)[u];
+                }
+            }
+        } else {
+            constexpr int kUnits = VPW * SA / 2;
+            constexpr int kPerSlot = SA / 2;
+#pragma unroll 1
+            for (int u = lane; u < (kUnits + 31) / 32 * 32; u += 32) {
+                const int vv = min(u / kPerSlot, VPW - 1);
+                const uint64_t d = __shfl_sync(kFull, dst, vv * LPV);
+                if (u < kUnits && d != 0)
+                    reinterpret_cast<uint16_t*>(d)[u - vv * kPerSlot] = reinterpret_cast<const uint16_t*>(stage)[u];
+            }
         }
         __syncwarp();
     };
@@ -513,6 +539,19 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const uint16_t* k, 
     const FastDiv div_h = make_fast_div(static_cast<uint32_t>(c.num_kv_heads));
     const FastDiv div_bs = make_fast_div(static_cast<uint32_t>(c.block_size));
     const int narrow = vecs < (int64_t{1} << 32) ? 1 : 0;
+    // whole-token rows: the widest unit that the row size, the cache base and
+    // the block stride allow (0: the 2-byte scatter)
+    int row_unit = 0;
+    if (VPW % c.num_kv_heads == 0) {
+        const int64_t row = static_cast<int64_t>(c.num_kv_heads) * Slot<D, KB, VB>::kAligned;
+        const uint64_t base = reinterpret_cast<uint64_t>(c.data);
+        for (int u : {16, 8, 4}) {
+            if (row % u == 0 && base % u == 0 && c.block_stride % u == 0) {
+                row_unit = u;
+                break;
+            }
+        }
+    }
     if (rm != nullptr) {
         RingMap r = *rm;
         int g = grid;
@@ -528,7 +567,7 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const uint16_t* k, 
             g = static_cast<int>(want_step < cap ? want_step : cap);
         }
         store_kernel<D, KB, VB, true><<<g, kStoreWarps * 32, 0, stream>>>(p, c, k, v, num_tokens, nullptr, r, div_h,
-                                                                          div_bs, narrow);
+                                                                          div_bs, narrow, row_unit);
         return cudaGetLastError();
     }
     const int ring_bytes = KB != 8 ? kStoreWarps * 4 * VPW * D * 2 : 0;
@@ -536,7 +575,7 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const uint16_t* k, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ring_bytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, kStoreWarps * 32, ring_bytes, stream>>>(p, c, k, v, num_tokens, slot_mapping, RingMap{}, div_h,
-                                                         div_bs, narrow);
+                                                         div_bs, narrow, row_unit);
     return cudaGetLastError();
 }
 
