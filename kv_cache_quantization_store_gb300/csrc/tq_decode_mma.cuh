@@ -90,6 +90,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Four e4m3 codes (a 32-bit word) -> two f16x2: lo from bytes 0-1, hi from bytes 2-3.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n .reg .b16 l16, h16;\n mov.b32 {l16, h16}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l16;\n"
+        " cvt.rn.f16x2.e4m3x2 %1, h16;\n}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
@@ -522,16 +530,9 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
             // of the 4 dims this lane covers at k-step j
             uint32_t af[4];
             if constexpr (KB == 8) {
-                // unit j: 4 FP8 codes
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
-                        static_cast<__nv_fp8x2_storage_t>((kw0[j] >> (16 * e)) & 0xffffu), __NV_E4M3);
-                    const __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(
-                        static_cast<__nv_fp8x2_storage_t>((kw1[j] >> (16 * e)) & 0xffffu), __NV_E4M3);
-                    af[2 * e] = static_cast<uint32_t>(h0.x) | (static_cast<uint32_t>(h0.y) << 16);
-                    af[2 * e + 1] = static_cast<uint32_t>(h1.x) | (static_cast<uint32_t>(h1.y) << 16);
-                }
+                // unit j: 4 FP8 codes; each 16-bit half is one e4m3 pair -> f16x2
+                e4m3x4_to_f16x2(kw0[j], af[0], af[2]);
+                e4m3x4_to_f16x2(kw1[j], af[1], af[3]);
             } else if constexpr (KB == 4) {
                 // unit j: two pair codes, one per byte, moved to bit 7 (table rows of 128 bytes)
                 af[0] = ld32(lut + (((kw0[j] << 7) & 0x7F80u) | lane4));
