@@ -34,9 +34,27 @@ __device__ __forceinline__ uint64_t get_bytes(const uint8_t* p) {
     }
 }
 
+// Two floats -> bf16x2 (round to nearest even; lo in the low half).
 __device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two e4m3 codes (the low 16 bits of w; byte 0 -> low half) -> bf16x2.  The
+// e4m3 values are exact in f16, f32 and bf16, so no step rounds.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n .reg .b16 p, l, h;\n .reg .b32 hx;\n .reg .f32 fl, fh;\n"
+        " cvt.u16.u32 p, %1;\n"
+        " cvt.rn.f16x2.e4m3x2 hx, p;\n"
+        " mov.b32 {l, h}, hx;\n"
+        " cvt.f32.f16 fl, l;\n"
+        " cvt.f32.f16 fh, h;\n"
+        " cvt.rn.bf16x2.f32 %0, fh, fl;\n}\n"
+        : "=r"(r)
+        : "r"(w));
+    return r;
 }
 
 template <int D, int KB, int VB>
@@ -106,9 +124,7 @@ dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict
                 const uint64_t b = get_bytes<8>(slot + 8 * (part + LPV * j));
                 uint32_t w[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    w[q] = bf16_pair(e4m3_to_float(static_cast<uint32_t>(b >> (16 * q)) & 0xffu),
-                                     e4m3_to_float(static_cast<uint32_t>(b >> (16 * q + 8)) & 0xffu));
+                for (int q = 0; q < 4; ++q) w[q] = e4m3x2_to_bf16x2(static_cast<uint32_t>(b >> (16 * q)));
                 if (ok) kdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
             }
         } else {
