@@ -662,21 +662,23 @@ cudaError_t launch_ring_partial(const LayerParams& p, const uint16_t* q, const R
 }  // namespace
 
 cudaError_t launch_combine(const float* partials, float* out, int num_seqs, int num_q_heads, int d,
-                           int num_splits, cudaStream_t stream) {
+                           int num_splits, cudaStream_t stream, bool after_decode_kernel) {
     dim3 cgrid(static_cast<unsigned>(num_q_heads), static_cast<unsigned>(num_seqs));
     if (d > 256 || d % 2 != 0) return cudaErrorInvalidValue;
     // about 8 splits per warp, at most kCombineMaxWarps warps; with one warp
     // per (sequence, head), kCombineMaxWarps of them share a CTA
     int nw = (num_splits + 7) / 8;
     nw = nw < 1 ? 1 : (nw > kCombineMaxWarps ? kCombineMaxWarps : nw);
-    // Launched with programmatic stream serialisation: its CTAs may become
-    // resident while the decode grid finishes, and wait for it on the device.
+    // Right after the decode kernel it is launched with programmatic stream
+    // serialisation: its CTAs may become resident while the decode grid
+    // finishes, and wait for it on the device.  After an event wait (the
+    // ring's join) it is launched plainly.
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = after_decode_kernel ? 1 : 0;
     cfg.stream = stream;
     cfg.dynamicSmemBytes = 0;
     int one_warp = 0;
@@ -853,7 +855,7 @@ cudaError_t launch_decode(const LayerParams& p, const CacheGeom& c, const uint16
         if (e == cudaSuccess) e = er;
     }
     if (e != cudaSuccess) return e;
-    return launch_combine(partials, out, num_seqs, num_q_heads, p.d, plan.slot_stride, stream);
+    return launch_combine(partials, out, num_seqs, num_q_heads, p.d, plan.slot_stride, stream, side == nullptr);
 }
 
 }  // namespace tq

@@ -98,8 +98,10 @@ cudaError_t launch_decode_mma(const LayerParams& p, const CacheGeom& c, const ui
                               const int32_t* seq_lens, int max_seq_len, float sm_scale, const DecodePlan& plan,
                               int ring_tokens, void* workspace, cudaStream_t stream);
 // Log-sum-exp merge of the partials [S, Hq, slots, d + 2] into out [S, Hq, d].
+// after_decode_kernel: the previous launch on the stream is the decode
+// kernel (programmatic dependent launch applies).
 cudaError_t launch_combine(const float* partials, float* out, int num_seqs, int num_q_heads, int d,
-                           int slots, cudaStream_t stream);
+                           int slots, cudaStream_t stream, bool after_decode_kernel);
 
 cudaError_t launch_dequant(const LayerParams& p, const CacheGeom& c, const int32_t* block_table,
                            int max_blocks_per_seq, const int32_t* cu_seqlens, int num_seqs,
