@@ -18,6 +18,14 @@ namespace tq {
 namespace {
 
 constexpr int kDqWarps = 8;
+// Grid sizing: with MSE keys a block's warps take up to kDqIters grid-stride
+// steps each, so that fewer, longer-lived blocks share the cost of the
+// per-block table set-up, while the grid still spans kDqMinWaves waves of
+// kDqBlocksPerSm resident blocks (256 threads at up to 64 registers).  FP8
+// keys have no set-up to share and keep one step per warp.
+constexpr int kDqIters = 4;
+constexpr int kDqBlocksPerSm = 4;
+constexpr int kDqMinWaves = 4;
 
 // Reads NB bytes (3, 4 or 8) at a 2-byte aligned global address + byte offset
 // `off` (even for NB = 4 and 8) as the low-order bytes of a 64-bit word.
@@ -181,10 +189,15 @@ dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict
 template <int D, int KB, int VB>
 cudaError_t launch(const LayerParams& p, const CacheGeom& c, const int32_t* bt, int max_blocks,
                    const int32_t* cu, int num_seqs, int max_seq_len, uint16_t* k_out, uint16_t* v_out,
-                   cudaStream_t stream) {
+                   int sm_count, cudaStream_t stream) {
     constexpr int VPW = LaneSplit<D>::kVPW;
     const int64_t vecs = static_cast<int64_t>(max_seq_len) * c.num_kv_heads;
     int64_t gx = (vecs + VPW * kDqWarps - 1) / (VPW * kDqWarps);
+    const int64_t wave_blocks = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * kDqBlocksPerSm * kDqMinWaves;
+    int64_t iters = gx * num_seqs / wave_blocks;
+    constexpr int64_t kMaxIters = KB == 8 ? 1 : kDqIters;
+    iters = iters < 1 ? 1 : (iters > kMaxIters ? kMaxIters : iters);
+    gx = (gx + iters - 1) / iters;
     if (gx > 1024) gx = 1024;
     if (gx < 1) gx = 1;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(num_seqs));
@@ -198,14 +211,14 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const int32_t* bt, 
 
 template <int D>
 cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const int32_t* bt, int mb,
-                          const int32_t* cu, int ns, int msl, uint16_t* ko, uint16_t* vo, cudaStream_t st) {
+                          const int32_t* cu, int ns, int msl, uint16_t* ko, uint16_t* vo, int sms, cudaStream_t st) {
     const int kb = p.kbits, vb = p.vbits;
-    if (kb == 3 && vb == 3) return launch<D, 3, 3>(p, c, bt, mb, cu, ns, msl, ko, vo, st);
-    if (kb == 3 && vb == 4) return launch<D, 3, 4>(p, c, bt, mb, cu, ns, msl, ko, vo, st);
-    if (kb == 4 && vb == 3) return launch<D, 4, 3>(p, c, bt, mb, cu, ns, msl, ko, vo, st);
-    if (kb == 4 && vb == 4) return launch<D, 4, 4>(p, c, bt, mb, cu, ns, msl, ko, vo, st);
-    if (kb == 8 && vb == 3) return launch<D, 8, 3>(p, c, bt, mb, cu, ns, msl, ko, vo, st);
-    if (kb == 8 && vb == 4) return launch<D, 8, 4>(p, c, bt, mb, cu, ns, msl, ko, vo, st);
+    if (kb == 3 && vb == 3) return launch<D, 3, 3>(p, c, bt, mb, cu, ns, msl, ko, vo, sms, st);
+    if (kb == 3 && vb == 4) return launch<D, 3, 4>(p, c, bt, mb, cu, ns, msl, ko, vo, sms, st);
+    if (kb == 4 && vb == 3) return launch<D, 4, 3>(p, c, bt, mb, cu, ns, msl, ko, vo, sms, st);
+    if (kb == 4 && vb == 4) return launch<D, 4, 4>(p, c, bt, mb, cu, ns, msl, ko, vo, sms, st);
+    if (kb == 8 && vb == 3) return launch<D, 8, 3>(p, c, bt, mb, cu, ns, msl, ko, vo, sms, st);
+    if (kb == 8 && vb == 4) return launch<D, 8, 4>(p, c, bt, mb, cu, ns, msl, ko, vo, sms, st);
     return cudaErrorInvalidValue;
 }
 
@@ -213,13 +226,13 @@ cudaError_t dispatch_bits(const LayerParams& p, const CacheGeom& c, const int32_
 
 cudaError_t launch_dequant(const LayerParams& p, const CacheGeom& c, const int32_t* block_table,
                            int max_blocks_per_seq, const int32_t* cu_seqlens, int num_seqs, int max_seq_len,
-                           uint16_t* k_out, uint16_t* v_out, cudaStream_t stream) {
+                           uint16_t* k_out, uint16_t* v_out, int sm_count, cudaStream_t stream) {
     switch (p.d) {
-        case 16: return dispatch_bits<16>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, stream);
-        case 32: return dispatch_bits<32>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, stream);
-        case 64: return dispatch_bits<64>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, stream);
-        case 128: return dispatch_bits<128>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, stream);
-        case 256: return dispatch_bits<256>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, stream);
+        case 16: return dispatch_bits<16>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, sm_count, stream);
+        case 32: return dispatch_bits<32>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, sm_count, stream);
+        case 64: return dispatch_bits<64>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, sm_count, stream);
+        case 128: return dispatch_bits<128>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, sm_count, stream);
+        case 256: return dispatch_bits<256>(p, c, block_table, max_blocks_per_seq, cu_seqlens, num_seqs, max_seq_len, k_out, v_out, sm_count, stream);
         default: return cudaErrorInvalidValue;
     }
 }

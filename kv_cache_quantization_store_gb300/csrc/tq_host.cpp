@@ -480,9 +480,12 @@ tq_status tq_dequant(const tq_config* cfg, const tq_cache* cache, const int32_t*
         return fail(TQ_ERR_INVALID_ARG, "block_table, cu_seqlens, k_out and v_out must not be NULL");
     if (!aligned(k_out_dev, 16) || !aligned(v_out_dev, 16))
         return fail(TQ_ERR_INVALID_ARG, "k_out and v_out must be 16-byte aligned");
+    int sms = 0;
+    st = sm_count(&sms);
+    if (st != TQ_OK) return st;
     const cudaError_t e = tq::launch_dequant(lp, g, block_table_dev, max_blocks_per_seq, cu_seqlens_dev, num_seqs,
                                              max_seq_len, static_cast<uint16_t*>(k_out_dev),
-                                             static_cast<uint16_t*>(v_out_dev), static_cast<cudaStream_t>(stream));
+                                             static_cast<uint16_t*>(v_out_dev), sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tq_dequant launch");
     return TQ_OK;
 }

@@ -105,7 +105,7 @@ cudaError_t launch_combine(const float* partials, float* out, int num_seqs, int 
 
 cudaError_t launch_dequant(const LayerParams& p, const CacheGeom& c, const int32_t* block_table,
                            int max_blocks_per_seq, const int32_t* cu_seqlens, int num_seqs,
-                           int max_seq_len, uint16_t* k_out, uint16_t* v_out, cudaStream_t stream);
+                           int max_seq_len, uint16_t* k_out, uint16_t* v_out, int sm_count, cudaStream_t stream);
 
 // Records the text tq_last_error() returns on this host thread.
 void set_last_error(const char* msg);
