@@ -62,6 +62,9 @@ typedef enum tq_status {
 
 #define TQ_MAX_HEAD_DIM 256
 #define TQ_MAX_CENTROIDS 16
+/* most sequences of one decode or dequant call: their kernels take one grid
+ * row per sequence (TQ_ERR_UNSUPPORTED above) */
+#define TQ_MAX_SEQS 65535
 
 /* Bits a kernel ORs into *tq_cache.error_flags when it meets bad input.  The
  * offending access is skipped; nothing outside the given buffers is touched. */
@@ -202,8 +205,8 @@ TQ_API size_t tq_decode_workspace_size(const tq_config* cfg, int32_t num_seqs, i
  *   out_dev: fp32 [num_seqs, num_q_heads, head_dim]
  *   workspace_dev: >= tq_decode_workspace_size(...) bytes, 16-byte aligned,
  *                  zero-filled before first use (see above)
- * Requires block_size % 16 == 0 and a 16-byte aligned cache.  Concurrent
- * calls sharing one workspace race.
+ * Requires block_size % 16 == 0, a 16-byte aligned cache and num_seqs <=
+ * TQ_MAX_SEQS.  Concurrent calls sharing one workspace race.
  */
 TQ_API tq_status tq_decode_attention(const tq_config* cfg, const void* q_dev, int32_t num_seqs,
                               int32_t num_q_heads, const tq_cache* cache,
@@ -221,6 +224,7 @@ TQ_API tq_status tq_decode_attention(const tq_config* cfg, const void* q_dev, in
  * v_hat = scale * code + zero, each computed in fp32 and rounded to bf16.
  *   cu_seqlens_dev: int32 [num_seqs + 1], host-visible bound max_seq_len on
  *   every sequence length.
+ * num_seqs <= TQ_MAX_SEQS.
  */
 TQ_API tq_status tq_dequant(const tq_config* cfg, const tq_cache* cache, const int32_t* block_table_dev,
                      int32_t max_blocks_per_seq, const int32_t* cu_seqlens_dev, int32_t num_seqs,

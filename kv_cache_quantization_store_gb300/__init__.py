@@ -22,7 +22,7 @@ __all__ = [
     "tq_decode_workspace_size", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_dequant",
     "tq_ring_workspace_size", "tq_ring_append", "tq_ring_step", "tq_decode_ring_workspace_size",
     "tq_decode_attention_ring",
-    "new_ring", "tq_status_str", "TQ_NOALLOC_SCRATCH_BYTES", "TQ_RING_TOKENS",
+    "new_ring", "tq_status_str", "TQ_NOALLOC_SCRATCH_BYTES", "TQ_RING_TOKENS", "TQ_MAX_SEQS",
     "new_paged_cache", "tq_hybrid_page", "PRESETS",
 ]
 
@@ -35,6 +35,7 @@ TQ_FLAG_BLOCK_OUT_OF_RANGE = 2
 TQ_FLAG_SEQ_TOO_LONG = 4
 TQ_FLAG_WAIT_TIMEOUT = 8
 TQ_RING_TOKENS = 128  # include/tq.h
+TQ_MAX_SEQS = 65535  # include/tq.h: sequences of one decode or dequant call
 
 _PKG = Path(__file__).resolve().parent
 

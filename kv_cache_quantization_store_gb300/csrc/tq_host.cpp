@@ -316,6 +316,8 @@ tq_status decode_common(const tq_config* cfg, const void* q_dev, int32_t num_seq
     if (st != TQ_OK) return st;
     if (num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq <= 0 || num_splits < 0)
         return fail(TQ_ERR_INVALID_ARG, "negative size argument");
+    if (num_seqs > TQ_MAX_SEQS)
+        return fail(TQ_ERR_UNSUPPORTED, "num_seqs (%d) above %d (one grid row per sequence)", num_seqs, TQ_MAX_SEQS);
     if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0)
         return fail(TQ_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
                     num_q_heads, cache->num_kv_heads);
@@ -475,6 +477,8 @@ tq_status tq_dequant(const tq_config* cfg, const tq_cache* cache, const int32_t*
     if (st != TQ_OK) return st;
     if (num_seqs < 0 || max_seq_len < 0 || max_blocks_per_seq <= 0)
         return fail(TQ_ERR_INVALID_ARG, "negative size argument");
+    if (num_seqs > TQ_MAX_SEQS)
+        return fail(TQ_ERR_UNSUPPORTED, "num_seqs (%d) above %d (one grid row per sequence)", num_seqs, TQ_MAX_SEQS);
     if (num_seqs == 0 || max_seq_len == 0) return TQ_OK;
     if (block_table_dev == nullptr || cu_seqlens_dev == nullptr || k_out_dev == nullptr || v_out_dev == nullptr)
         return fail(TQ_ERR_INVALID_ARG, "block_table, cu_seqlens, k_out and v_out must not be NULL");

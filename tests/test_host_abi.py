@@ -169,6 +169,34 @@ def test_decode_argument_errors(libtq):
     assert call(_cache(heads=1), hq=16) == 3         # GQA group above 8
 
 
+def test_sequence_limit(libtq):
+    """Decode and dequant take one grid row per sequence: above TQ_MAX_SEQS
+    they return TQ_ERR_UNSUPPORTED before anything is enqueued; at the limit
+    the next check (a NULL pointer here) answers."""
+    from kv_cache_quantization_store_gb300 import TQ_MAX_SEQS, tq_config_init
+
+    text = HEADER.read_text()
+    assert int(re.search(r"#define TQ_MAX_SEQS (\d+)", text).group(1)) == TQ_MAX_SEQS == 65535
+    cfg = tq_config_init(64, 3, 4)
+    c = _cache()
+
+    def decode(seqs, q=64):
+        return libtq.tq_decode_attention(ctypes.byref(cfg), q, seqs, 2, ctypes.byref(c), 64, 4, 64, 64, 0.0,
+                                         0, 64, 64, 1 << 20, None)
+
+    def ring_decode(seqs, q=64):
+        return libtq.tq_decode_attention_ring(ctypes.byref(cfg), q, seqs, 2, ctypes.byref(c), 64, 4, 64, 64, 0.0,
+                                              0, 64, 64, 128, 64, 64, 1 << 20, None)
+
+    def dequant(seqs, k=64):
+        return libtq.tq_dequant(ctypes.byref(cfg), ctypes.byref(c), 64, 4, 64, seqs, 16, k, 64, None)
+
+    for fn in (decode, ring_decode, dequant):
+        assert fn(TQ_MAX_SEQS + 1) == 3, fn.__name__
+        assert b"65535" in libtq.tq_last_error()
+        assert fn(TQ_MAX_SEQS, None) == 1, fn.__name__
+
+
 def test_status_strings(libtq):
     from kv_cache_quantization_store_gb300 import tq_status_str
 
