@@ -250,6 +250,15 @@ def _dev(t: torch.Tensor, dtype, name: str):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _token_rows(t: torch.Tensor, name: str, heads: int, d: int, ring: bool = False):
+    """Shape check of K/V rows: [T, H, d], or [S, R, H, d] for a ring.  The
+    kernels index these rows with the cache's H and the config's d."""
+    want = 4 if ring else 3
+    if t.dim() != want or tuple(t.shape[-2:]) != (heads, d):
+        lead = "[S, R, " if ring else "["
+        raise ValueError(f"{name} must be {lead}num_kv_heads={heads}, head_dim={d}], got {tuple(t.shape)}")
+
+
 def tq_store_kv(cfg: TqConfig, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                 cache: PagedCache, stream=None):
     """k, v: bf16 [T, H, d]; slot_mapping: int64 [T] (negative = skip)."""
@@ -335,6 +344,10 @@ def tq_ring_append(cfg: TqConfig, k: torch.Tensor, v: torch.Tensor, cu_new: torc
         raise ValueError("cu_new must be [S + 1] and block_table [S, max_blocks]")
     if ring_k.shape != ring_v.shape or ring_k.dim() != 4 or ring_k.shape[0] != num_seqs:
         raise ValueError("ring_k and ring_v must be [S, R, H, d]")
+    _token_rows(ring_k, "ring_k", cache.num_kv_heads, cfg.head_dim, ring=True)
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    _token_rows(k, "k", cache.num_kv_heads, cfg.head_dim)
     desc = cache.descriptor()
     _check(lib().tq_ring_append(
         ctypes.byref(cfg), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"), k.shape[0],
@@ -351,10 +364,12 @@ def tq_ring_step(cfg: TqConfig, k: torch.Tensor, v: torch.Tensor, seq_lens: torc
     num_seqs = seq_lens.shape[0]
     if k.dim() != 3 or k.shape[0] != num_seqs or v.shape != k.shape:
         raise ValueError("k and v must be [S, H, d] with one row per sequence")
+    _token_rows(k, "k", cache.num_kv_heads, cfg.head_dim)
     if block_table.dim() != 2 or block_table.shape[0] != num_seqs:
         raise ValueError("block_table must be [S, max_blocks]")
     if ring_k.shape != ring_v.shape or ring_k.dim() != 4 or ring_k.shape[0] != num_seqs:
         raise ValueError("ring_k and ring_v must be [S, R, H, d]")
+    _token_rows(ring_k, "ring_k", cache.num_kv_heads, cfg.head_dim, ring=True)
     desc = cache.descriptor()
     _check(lib().tq_ring_step(
         ctypes.byref(cfg), _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"), num_seqs,
@@ -384,6 +399,7 @@ def tq_decode_attention_ring(cfg: TqConfig, q: torch.Tensor, cache: PagedCache, 
         raise ValueError("block_table must be [S, max_blocks] and seq_lens [S]")
     if ring_k.shape != ring_v.shape or ring_k.dim() != 4 or ring_k.shape[0] != q.shape[0]:
         raise ValueError("ring_k and ring_v must be [S, R, H, d]")
+    _token_rows(ring_k, "ring_k", cache.num_kv_heads, cfg.head_dim, ring=True)
     desc = cache.descriptor()
     _check(lib().tq_decode_attention_ring(
         ctypes.byref(cfg), _dev(q, torch.bfloat16, "q"), q.shape[0], q.shape[1], ctypes.byref(desc),
@@ -396,9 +412,14 @@ def tq_decode_attention_ring(cfg: TqConfig, q: torch.Tensor, cache: PagedCache, 
 
 def tq_dequant(cfg: TqConfig, cache: PagedCache, block_table: torch.Tensor, cu_seqlens: torch.Tensor,
                max_seq_len: int, k_out: torch.Tensor, v_out: torch.Tensor, stream=None):
-    """k_out, v_out: bf16 [cu_seqlens[-1], H, d]; cu_seqlens int32 [S + 1]."""
+    """k_out, v_out: bf16 [cu_seqlens[-1], H, d]; cu_seqlens int32 [S + 1].
+    The row count of k_out and v_out is the caller's to get right (reading
+    cu_seqlens[-1] here would synchronise the stream)."""
     if block_table.dim() != 2 or cu_seqlens.shape != (block_table.shape[0] + 1,):
         raise ValueError("block_table must be [S, max_blocks] and cu_seqlens [S + 1]")
+    if v_out.shape != k_out.shape:
+        raise ValueError("k_out and v_out must have the same shape")
+    _token_rows(k_out, "k_out", cache.num_kv_heads, cfg.head_dim)
     desc = cache.descriptor()
     _check(lib().tq_dequant(
         ctypes.byref(cfg), ctypes.byref(desc), _dev(block_table, torch.int32, "block_table"),

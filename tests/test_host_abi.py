@@ -267,3 +267,38 @@ def test_ring_decode_workspace_has_one_more_partial(libtq):
     up = lambda x: -(-x // 256) * 256
     assert plain == up(s * hq * splits * 66 * 4)
     assert ring == up(s * hq * (splits + 1) * 66 * 4)
+
+
+def test_binding_checks_row_shapes(libtq):
+    """The binding rejects K/V rows whose trailing dims are not the cache's
+    (num_kv_heads, head_dim) before anything reaches the library: the
+    kernels index those rows with the cache's H and the config's d."""
+    import torch
+
+    import kv_cache_quantization_store_gb300 as tq
+
+    cfg = tq.tq_config_init(64, 3, 4)
+    cache = tq.new_paged_cache(cfg, 2, 16, 2, 0, device="cpu", with_flags=False)
+    table = torch.zeros((1, 2), dtype=torch.int32)
+    cu = torch.tensor([0, 4], dtype=torch.int32)
+    lens = torch.zeros(1, dtype=torch.int32)
+    rows = lambda *shape: torch.zeros(shape, dtype=torch.bfloat16)
+
+    with pytest.raises(ValueError, match="k_out"):
+        tq.tq_dequant(cfg, cache, table, cu, 4, rows(4, 2 * 64), rows(4, 2 * 64))    # flattened rows
+    with pytest.raises(ValueError, match="k_out"):
+        tq.tq_dequant(cfg, cache, table, cu, 4, rows(4, 1, 64), rows(4, 1, 64))      # wrong head count
+    with pytest.raises(ValueError, match="same shape"):
+        tq.tq_dequant(cfg, cache, table, cu, 4, rows(4, 2, 64), rows(3, 2, 64))
+    ring_ok, ring_bad = rows(1, 8, 2, 64), rows(1, 8, 2, 32)
+    with pytest.raises(ValueError, match="ring_k"):
+        tq.tq_ring_step(cfg, rows(1, 2, 64), rows(1, 2, 64), lens, ring_bad, ring_bad, cache, table)
+    with pytest.raises(ValueError, match="k must be"):
+        tq.tq_ring_step(cfg, rows(1, 4, 32), rows(1, 4, 32), lens, ring_ok, ring_ok, cache, table)
+    with pytest.raises(ValueError, match="k must be"):
+        tq.tq_ring_append(cfg, rows(3, 2, 32), rows(3, 2, 32), cu, lens, ring_ok, ring_ok, cache, table,
+                          torch.zeros(64, dtype=torch.uint8))
+    q, out = rows(1, 4, 64), torch.zeros((1, 4, 64), dtype=torch.float32)
+    with pytest.raises(ValueError, match="ring_k"):
+        tq.tq_decode_attention_ring(cfg, q, cache, table, lens, 16, ring_bad, ring_bad, out,
+                                    torch.zeros(64, dtype=torch.uint8))
