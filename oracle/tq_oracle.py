@@ -617,7 +617,8 @@ def dequant_cache(layer: Layer, cache: PagedCache, block_table: np.ndarray, cu_s
 
     Token j of sequence s lands in row cu_seqlens[s] + j.  Returns
     (k [rows, H, d], v [rows, H, d]) as bf16 values held in float32: keys
-    rounded from fp64, values from the fp32 reconstruction.
+    rounded from fp64 to fp32 and then to bf16, values from the fp32
+    reconstruction.
     """
     cfg = layer.cfg
     rows = int(cu_seqlens[-1])

@@ -378,6 +378,45 @@ def test_dequant_reconstruction_and_nc():
     assert rel.mean() < 0.015
 
 
+def test_dequant_cache_varlen_layout_from_hand_built_slots():
+    """dequant_cache against slots written byte by byte: FP8 keys decoded by
+    torch's float8_e4m3fn, values fp32(scale) * code + fp32(zero) with one
+    fp32 rounding (the product is exact) and torch's bf16 rounding, and token
+    j of sequence s in row cu_seqlens[s] + j through a permuted block table
+    and a padded block stride."""
+    import torch
+
+    d, h_n, bs = 16, 2, 4
+    cfg = O.Config(head_dim=d, key_quant_bits=8, value_quant_bits=4)
+    layer = O.make_layer(cfg, 0)
+    slot_bytes = 16 + 8 + 4
+    assert cfg.slot_size_aligned == slot_bytes
+    stride = bs * h_n * slot_bytes + 32
+    cache = O.new_cache(cfg, 8, bs, h_n, block_stride=stride)
+    lens = [5, 11]
+    table = np.array([[6, 1, 0, 0], [3, 7, 0, 5]])
+    cu = np.array([0, 5, 16])
+    s16, z16 = np.float16(0.1), np.float16(0.3)
+    want_k = np.zeros((16, h_n, d), dtype=np.float32)
+    want_v = np.zeros((16, h_n, d), dtype=np.float32)
+    for s, n in enumerate(lens):
+        for j in range(n):
+            for h in range(h_n):
+                row = cu[s] + j
+                kb = np.array([(7 * row + 5 * h + 3 * i) % 0x77 for i in range(d)], dtype=np.uint8)
+                codes = np.array([(row + 3 * h + i) % 16 for i in range(d)])
+                packed = np.array([codes[2 * b] | (codes[2 * b + 1] << 4) for b in range(d // 2)], dtype=np.uint8)
+                tail = np.frombuffer(np.array([s16, z16], dtype="<f2").tobytes(), dtype=np.uint8)
+                off = table[s, j // bs] * stride + ((j % bs) * h_n + h) * slot_bytes
+                cache.data[off:off + slot_bytes] = np.concatenate([kb, packed, tail])
+                want_k[row, h] = torch.from_numpy(kb).view(torch.float8_e4m3fn).float().numpy()
+                exact32 = np.float32(s16) * codes.astype(np.float32) + np.float32(z16)
+                want_v[row, h] = torch.from_numpy(exact32).to(torch.bfloat16).float().numpy()
+    k_out, v_out = O.dequant_cache(layer, cache, table, cu)
+    np.testing.assert_array_equal(k_out, want_k)
+    np.testing.assert_array_equal(v_out, want_v)
+
+
 # -- decode ---------------------------------------------------------------------
 
 def _tiny_cache(layer, n_tok, h_n, k, v):
