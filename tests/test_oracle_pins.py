@@ -355,6 +355,13 @@ def test_cache_scatter_roundtrip():
     keep = np.arange(40) != 7
     np.testing.assert_array_equal(got[keep], want[keep])
     assert np.all(got[7] == 0)
+    # the same bytes at addresses worked out by hand: block table[t // 8] at
+    # its (padded) stride, then position t % 8 and head h in [B, H, slot] order
+    sb = cfg.slot_size_aligned
+    for t in np.flatnonzero(keep):
+        for h in range(2):
+            off = table[0, t // 8] * cache.block_stride + ((t % 8) * 2 + h) * sb
+            np.testing.assert_array_equal(cache.data[off:off + sb], want[t, h])
 
 
 def test_dequant_reconstruction_and_nc():
