@@ -28,8 +28,12 @@ Pins (tests/test_oracle_pins.py): slot sizes and the compression column of
 the [TQC] preset table, the per-layer seed rule, published SplitMix64 test
 vectors, Sylvester-Hadamard orthogonality and the FWHT, Lloyd-Max fixed-point
 conditions plus Max's (1960) published N(0,1) quantiser tables and the 1-bit
-closed form sqrt(2/pi), exhaustive e4m3 encode against a brute-force nearest
-search, value-quantiser invariants, brute-force decode special cases,
+closed form sqrt(2/pi), fp32 centroids and boundaries against an
+independent 40-digit solve (boundaries: the correctly rounded exact
+midpoint, not the midpoint of the fp32 centroids), exhaustive e4m3 encode
+against a brute-force nearest search, value-quantiser invariants and
+hand-worked rows that fix its readings (codes against the fp16 scale and
+zero, ties to even), brute-force decode special cases,
 split invariance of the log-sum-exp merge, and for the ring: token-by-token
 appends equal one plain store of the whole blocks (bytes) with the rest
 verbatim in the ring, chunked appends equal single steps, and the ring

@@ -186,6 +186,72 @@ def test_lloyd_max_matches_max_1960_table():
         assert abs(mse - rows[(levels, "mse")][0]) / rows[(levels, "mse")][0] < 2e-3
 
 
+def _golden_codebook_rows():
+    rows = []
+    for line in golden_lines("codebook_fp32_d128_b3.txt"):
+        j, bits, mid, alt = (f.strip() for f in line.split("|"))
+        rows.append((int(j), int(bits, 16), mid, int(alt, 16)))
+    return rows
+
+
+def test_codebook_boundaries_round_the_exact_midpoint():
+    """fp32 boundaries are the correctly rounded exact midpoints of the scaled
+    Lloyd-Max centroids (d=128, 3 bits, tests/golden/codebook_fp32_d128_b3.txt,
+    derived with mpmath); the midpoint of the fp32 centroids differs."""
+    cb = O.codebook(128, 3)
+    got = cb.boundaries.view(np.uint32)
+    c32 = cb.centroids.astype(np.float64)
+    alt = (0.5 * (c32[:-1] + c32[1:])).astype(np.float32).view(np.uint32)
+    differs = 0
+    for j, bits, _, alt_bits in _golden_codebook_rows():
+        assert got[j] == bits, (j, hex(got[j]), hex(bits))
+        assert alt[j] == alt_bits, (j, hex(alt[j]), hex(alt_bits))
+        differs += alt_bits != bits
+    assert differs >= 1
+
+
+def _rn_fp32(x, mp):
+    """Correctly rounded fp32 of an mpmath value (ties to the even pattern)."""
+    f = np.float32(float(x))
+    cands = [np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf))]
+    dist = [abs(mp.mpf(float(c)) - x) for c in cands]
+    best = [c for c, dd in zip(cands, dist) if dd == min(dist)]
+    return best[0] if len(best) == 1 else [c for c in best if int(c.view(np.uint32)) % 2 == 0][0]
+
+
+@pytest.mark.parametrize("d,bits", [(64, 3), (128, 3), (128, 4), (256, 4)])
+def test_codebook_tables_against_high_precision_solve(d, bits):
+    """Independent 40-digit solve of the Lloyd-Max conditions for N(0,1)
+    (mpmath Newton, started at Max's 1960 values): the oracle's fp32
+    centroids and boundaries are its correct fp32 roundings."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 40
+    levels = 1 << bits
+    half = levels // 2
+    start = {8: [0.2451, 0.7560, 1.3440, 2.1520],
+             16: [0.1284, 0.3881, 0.6568, 0.9424, 1.2562, 1.6181, 2.0690, 2.7326]}[levels]
+
+    def conditions(*c):
+        edges = [mp.mpf(0)] + [(c[j] + c[j + 1]) / 2 for j in range(half - 1)] + [mp.inf]
+        res = []
+        for j in range(half):
+            a, b = edges[j], edges[j + 1]
+            pb = 0 if b == mp.inf else mp.npdf(b)
+            res.append(c[j] - (mp.npdf(a) - pb) / (mp.ncdf(b) - mp.ncdf(a)))
+        return res
+
+    sol = mp.findroot(conditions, [mp.mpf(x) for x in start])
+    pos = [sol[i] for i in range(half)]
+    sigma = 1 / mp.sqrt(d)
+    pos_bnd = [sigma * (pos[j] + pos[j + 1]) / 2 for j in range(half - 1)]
+    want_c = [-_rn_fp32(sigma * x, mp) for x in pos[::-1]] + [_rn_fp32(sigma * x, mp) for x in pos]
+    want_b = [-_rn_fp32(x, mp) for x in pos_bnd[::-1]] + [np.float32(0.0)] + [_rn_fp32(x, mp) for x in pos_bnd]
+    cb = O.codebook(d, bits)
+    np.testing.assert_array_equal(cb.centroids.view(np.uint32), np.array(want_c, dtype=np.float32).view(np.uint32))
+    np.testing.assert_array_equal(np.abs(cb.boundaries).view(np.uint32),
+                                  np.abs(np.array(want_b, dtype=np.float32)).view(np.uint32))
+
+
 def test_codebook_scaling_and_symmetry():
     for d, bits in ((64, 3), (128, 3), (128, 4), (256, 4)):
         cb = O.codebook(d, bits)
@@ -322,6 +388,21 @@ def test_value_quant_error_bound(bits):
     assert np.all(np.abs(v_hat - v) <= 0.5 * s + slack)
     # most vectors use both ends of the code range
     assert np.mean(codes.min(axis=1) == 0) > 0.9 and np.mean(codes.max(axis=1) == top) > 0.9
+
+
+def test_value_quant_readings_hand_worked():
+    """tests/golden/value_quant_readings.txt: codes decided against the fp16
+    scale and zero a reader sees, ties to even; each row also fails the
+    rejected reading it names."""
+    for line in golden_lines("value_quant_readings.txt"):
+        bits, vals, sbits, zbits, codes, rejected, _ = (f.strip() for f in line.split("|"))
+        v = np.array([[float(x) for x in vals.split()]], dtype=np.float32)
+        got_codes, scale, zero = O.encode_values(v, int(bits))
+        assert int(scale.view(np.uint16)[0]) == int(sbits, 16)
+        assert int(zero.view(np.uint16)[0]) == int(zbits, 16)
+        want = [int(x) for x in codes.split()]
+        np.testing.assert_array_equal(got_codes[0], want)
+        assert want != [int(x) for x in rejected.split()]
 
 
 # -- slots, cache and dequant -------------------------------------------------------
