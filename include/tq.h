@@ -351,8 +351,11 @@ TQ_API tq_status tq_hybrid_page(const tq_config* cfg, int32_t num_kv_heads, int3
  * GPU that loads the library holds until the process exits.  It allocates
  * nothing and calls no cudaMalloc or cudaFree.
  *   - Arguments, layouts and results are those of tq_decode_attention.
- *   - A decode whose workspace (tq_decode_workspace_size) exceeds the limit is
- *     rejected with TQ_ERR_WORKSPACE before anything is enqueued.
+ *   - With num_splits = 0, when the automatic split count's workspace
+ *     (tq_decode_workspace_size) exceeds the limit, the decode runs with the
+ *     largest split count that fits.  A decode that does not fit even with
+ *     one split, or with the caller's num_splits > 0, is rejected with
+ *     TQ_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) and caches it; make that first call before any
  *     stream capture.

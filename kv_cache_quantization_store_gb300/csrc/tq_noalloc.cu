@@ -57,8 +57,23 @@ tq_status tq_decode_attention_noalloc(const tq_config* cfg, const void* q_dev, i
                                       int32_t max_blocks_per_seq, const int32_t* seq_lens_dev, int32_t max_seq_len,
                                       float sm_scale, int32_t num_splits, float* out_dev, void* stream) {
     if (cache != nullptr && cfg != nullptr && num_seqs > 0 && num_q_heads > 0) {
-        const size_t need = tq_decode_workspace_size(cfg, num_seqs, num_q_heads, cache->num_kv_heads,
-                                                     cache->block_size, max_seq_len, num_splits);
+        size_t need = tq_decode_workspace_size(cfg, num_seqs, num_q_heads, cache->num_kv_heads,
+                                               cache->block_size, max_seq_len, num_splits);
+        if (need > kScratchBytes && num_splits == 0 && cfg->head_dim > 0) {
+            // The automatic split count does not fit: take the most splits
+            // whose partial states do fit (fewer splits only lengthen each
+            // CTA's share of the sequence; the result is the same decode).
+            const size_t per_split = static_cast<size_t>(num_seqs) * static_cast<size_t>(num_q_heads) *
+                                     (static_cast<size_t>(cfg->head_dim) + 2) * sizeof(float);
+            int32_t splits = static_cast<int32_t>(kScratchBytes / per_split);
+            while (splits >= 1) {
+                need = tq_decode_workspace_size(cfg, num_seqs, num_q_heads, cache->num_kv_heads, cache->block_size,
+                                                max_seq_len, splits);
+                if (need <= kScratchBytes) break;
+                --splits;
+            }
+            if (splits >= 1) num_splits = splits;
+        }
         if (need > kScratchBytes) {
             char msg[256];
             std::snprintf(msg, sizeof msg,

@@ -165,6 +165,30 @@ class Workload:
                 fill(c)
         return k, v
 
+    def kv_device(self, device, start: int = 0, stop: int | None = None):
+        """Keys and values of tokens [start, stop) drawn on the device: bf16
+        [n, H, d] each, with the workload's distribution (N(0,1), outlier
+        channels x10 or a per-token LogNormal(0, 0.5) factor) from torch's
+        generator seeded with (data_seed, STREAM_KV).  These are a second,
+        faster source of the same distribution for timing runs; they are not
+        the values ``kv`` returns."""
+        stop = self.num_tokens if stop is None else stop
+        n, h, d = stop - start, self.num_kv_heads, self.head_dim
+        g = torch.Generator(device=device)
+        g.manual_seed(self.data_seed * 1_000_003 + STREAM_KV * 7919 + start)
+        out = []
+        k_ch, v_ch = self._outlier_channels() if self.kv_mode == "outliers" else (None, None)
+        for ch in (k_ch, v_ch):
+            x = torch.randn((n, h, d), generator=g, device=device, dtype=torch.float32)
+            if self.kv_mode == "outliers":
+                for hh in range(h):
+                    x[:, hh, torch.as_tensor(ch[hh], device=device)] *= 10.0
+            elif self.kv_mode == "lognormal":
+                x *= torch.exp(0.5 * torch.randn((n, 1, 1), generator=g, device=device, dtype=torch.float32))
+            out.append(x.to(torch.bfloat16))
+            del x
+        return out[0], out[1]
+
     def q(self) -> np.ndarray:
         rng = np.random.default_rng([self.data_seed, STREAM_Q])
         x = rng.standard_normal((self.num_seqs, self.num_q_heads, self.head_dim), dtype=np.float32)

@@ -71,3 +71,89 @@ def test_full_size_store_and_decode(cuda_device, name):
     want = O.decode_attention(layer, q, ocache, table, wl.seq_lens, rows=rows)
     assert_rows_close(got, want, rows=rows)
     assert cache.error_flags() == 0
+
+
+#: configuration -> sampled sequences (one 16-token window per grid-stride range of each)
+DEQUANT_SAMPLES = {"c3": 2, "c4": 6, "c2": 2}
+
+
+def _dequant_steps(wl):
+    """Grid-stride ranges of the dequant's full-size launch, as positions:
+    (steps per warp, positions one step covers).  Mirrors the launch's
+    arithmetic in tq_dequant.cu (8 warps, 4 resident blocks per SM over at
+    least 4 waves, at most 4 steps with MSE keys, at most 1024 blocks per
+    sequence) for a 152-SM GB300."""
+    vpw = 32 // max(1, wl.head_dim // 32)  # vectors per warp: 32 / (d / min(d, 32))
+    vecs = int(wl.seq_lens.max()) * wl.num_kv_heads
+    gx = -(-vecs // (vpw * 8))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    iters = gx * wl.num_seqs // (sms * 4 * 4)
+    iters = max(1, min(1 if wl.key_bits == 8 else 4, iters))
+    gx = min(1024, max(1, -(-gx // iters)))
+    per_step = gx * 8 * vpw // wl.num_kv_heads
+    steps = -(-vecs // (gx * 8 * vpw))
+    return steps, per_step
+
+
+@pytest.mark.parametrize("name", list(DEQUANT_SAMPLES))
+def test_full_size_dequant(cuda_device, name):
+    """tq_dequant over the whole decode batch in its full-size launch shape
+    (several grid-stride steps per warp and the 1024-block cap at c3):
+    oracle-encoded slots at sampled positions, one 16-token window in each
+    grid-stride range of each sampled sequence, all KV heads, compared with
+    the oracle's dequant of the same bytes (values bit-exact, keys within one
+    bf16 ulp)."""
+    n_seq = DEQUANT_SAMPLES[name]
+    wl = W.named(name)
+    layer_idx = wl.layers[0]
+    layer = oracle_layer(wl, layer_idx)
+    cfg = host_cfg(wl)
+    h_n, d, slot_al = wl.num_kv_heads, wl.head_dim, cfg.slot_size_aligned
+    table, nblk = wl.layout()
+    cu = wl.cu_seqlens()
+    steps, per_step = _dequant_steps(wl)
+    if name in ("c3", "c4"):
+        assert steps >= 4, (name, steps)  # the multi-step path is the one under test
+    rng = np.random.default_rng(7000 + int(name[1]))
+    seqs = np.sort(rng.choice(wl.num_seqs, n_seq, replace=False))
+    ocache = O.new_cache(layer.cfg, nblk, wl.block_size, h_n, wl.block_stride)
+    picked = []  # (sequence, positions)
+    for s in seqs:
+        n = int(wl.seq_lens[s])
+        pos = []
+        for i in range(steps):
+            lo, hi = i * per_step, min(n, (i + 1) * per_step)
+            if hi - lo >= 16:
+                p0 = lo + 16 * int(rng.integers(0, (hi - lo) // 16))
+                pos.extend(range(p0, p0 + 16))
+        pos = np.array(pos, dtype=np.int64)
+        picked.append((int(s), pos))
+        k = np.concatenate([wl.kv(int(cu[s] + p), int(cu[s] + p + 16))[0] for p in pos[::16]])
+        v = np.concatenate([wl.kv(int(cu[s] + p), int(cu[s] + p + 16))[1] for p in pos[::16]])
+        ids = table[s][pos // wl.block_size].astype(np.int64) * wl.block_size + pos % wl.block_size
+        off = O.slot_offsets(ocache, ids)
+        for h in range(h_n):
+            slots, _ = O.encode_slots(layer, k[:, h], v[:, h])
+            ocache.data[(off[:, h][:, None] + np.arange(slot_al)).ravel()] = slots.ravel()
+    cache = tq.new_paged_cache(cfg, nblk, wl.block_size, h_n, layer_idx, block_stride=wl.block_stride,
+                               device=cuda_device)
+    cache.data.copy_(torch.from_numpy(ocache.data))
+    rows = int(cu[-1])
+    k_out = torch.full((rows, h_n, d), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+    v_out = torch.full_like(k_out, float("nan"))
+    tq.tq_dequant(cfg, cache, torch.from_numpy(table).to(cuda_device), torch.from_numpy(cu).to(cuda_device),
+                  int(wl.seq_lens.max()), k_out, v_out)
+    torch.cuda.synchronize()
+    assert cache.error_flags() == 0
+    for s, pos in picked:
+        r = torch.from_numpy(cu[s] + pos).to(cuda_device)
+        kg = k_out[r].float().cpu().numpy()
+        vg = v_out[r].float().cpu().numpy()
+        for h in range(h_n):
+            sl = O.read_slots(ocache, table[s], int(pos[-1]) + 1, h)[pos]
+            k_hat, _ = O.dequant_slots(layer, sl)
+            kw = O.bf16_round(k_hat.astype(np.float32))
+            vw = O.bf16_round(O.dequant_values_f32(layer, sl))
+            np.testing.assert_array_equal(vg[:, h], vw, err_msg=f"values, sequence {s} head {h}")
+            tol = np.abs(kw) * 2.0 ** -7 + 1e-6 * np.abs(kw).max(axis=-1, keepdims=True)
+            assert np.all(np.abs(kg[:, h] - kw) <= tol), f"keys, sequence {s} head {h}"

@@ -78,3 +78,35 @@ def test_noalloc_rejects_decode_beyond_scratch(cuda_device):
     assert b"no-allocation" in tq.lib().tq_last_error()
     torch.cuda.synchronize()
     assert not out.any()
+
+
+def test_noalloc_auto_split_count_shrinks_to_fit(cuda_device):
+    """With num_splits = 0, a batch whose automatic split count needs more
+    partial storage than the scratch holds runs with the most splits that
+    fit (here the c4 decode shape: 256 sequences x 16 query heads, d = 256),
+    and equals the workspace decode at that split count."""
+    wl = W.custom(256, 4, 4, True, 4, 16, 16, [48] * 256, 2800)
+    seqs, hq, max_len = 256, 16, 2048
+    cfg = tq.tq_config_init(wl.head_dim, wl.key_bits, wl.value_bits, wl.norm_correction)
+    auto = tq.tq_decode_workspace_size(cfg, seqs, hq, 4, 16, max_len, 0)
+    if auto <= tq.TQ_NOALLOC_SCRATCH_BYTES:
+        pytest.skip("the automatic split count fits the scratch on this device")
+    fit = tq.TQ_NOALLOC_SCRATCH_BYTES // (seqs * hq * (256 + 2) * 4)
+    assert fit >= 1
+    k, v = wl.kv()
+    cfg, cache = gpu_store(wl, 0, cuda_device, k, v)
+    qd = bf16(wl.q(), cuda_device)
+    table_np = np.zeros((seqs, max_len // 16), dtype=np.int32)  # room for max_len tokens, 48 used
+    table_np[:, :3] = wl.layout()[0]
+    table = torch.from_numpy(table_np).to(cuda_device)
+    lens = torch.from_numpy(wl.seq_lens.astype(np.int32)).to(cuda_device)
+    out = torch.full((seqs, hq, 256), float("nan"), dtype=torch.float32, device=cuda_device)
+    status = _noalloc_call(cfg, qd, cache, table, lens, max_len, out, 0)
+    assert status == 0, tq.lib().tq_last_error().decode()
+    ws = torch.zeros(tq.tq_decode_workspace_size(cfg, seqs, hq, 4, 16, max_len, int(fit)), dtype=torch.uint8,
+                     device=cuda_device)
+    ref = torch.empty_like(out)
+    tq.tq_decode_attention(cfg, qd, cache, table, lens, max_len, ref, ws, num_splits=int(fit))
+    torch.cuda.synchronize()
+    assert cache.error_flags() == 0
+    assert torch.equal(out, ref)
