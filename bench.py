@@ -41,6 +41,8 @@ import numpy as np
 ROOT = Path(__file__).resolve().parent
 METRIC = "fused TQ decode attn packed-KV HBM GB/s (% of peak); tq_store Mtok/s"
 FALLBACK_HBM_GBS = 6800.0
+#: seconds of untimed steps run under the clock sampler before the timed region
+PREROLL_S = 0.5
 
 
 def parse_args(argv=None):
@@ -57,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sub-workloads", default="c2,c3",
                     help="with the c4 workload: other configurations timed in the same run ('' to skip)")
+    ap.add_argument("--preroll-s", type=float, default=PREROLL_S,
+                    help="seconds of untimed steps under the clock sampler before the timed region")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the dequant, ring and comparator fields (profiling runs)")
     ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
@@ -367,7 +371,7 @@ def run_ours(args):
         # clock record covers the GPU under this load even when the timed
         # region is shorter than a sampling period
         load_start = time.time()
-        while time.time() - load_start < PREROLL_S:
+        while time.time() - load_start < args.preroll_s:
             step()
             torch.cuda.synchronize()
         barrier()
@@ -399,14 +403,15 @@ def run_ours(args):
     # ---- end to end through host buffers ---------------------------------------
     e2e = run_e2e(args, tq, wl, cfg, caches, k_new, v_new, slots_new, q, table, lens, max_len, ws, outs, stream,
                   packed, dev)
-    dq = ring = None
+    dq = ring = comparator = None
     if not args.no_extras:
         dq = measure_dequant(tq, wl, cfg, caches[0], table, max_len, dev, stream, peak)
         ring = measure_ring(tq, wl, cfg, caches[0], table, k_all, v_all, q, max_len, dev, stream)
+        comparator = measure_comparator(tq, wl, cfg, caches[0], table, q, max_len, dev, stream, dec_avg_s * 1e6)
     subs = {}
     if wl.name == "c4" and args.sub_workloads:
         for name in [x for x in args.sub_workloads.split(",") if x]:
-            subs[name] = measure_workload(name, tq, dev, stream, peak)
+            subs[name] = measure_workload(name, tq, dev, stream, peak, comparator=not args.no_extras)
 
     clk = clocks.summary(load_start, (host_t0, host_t1))
     result = {
@@ -439,6 +444,8 @@ def run_ours(args):
         result["dequant"] = dq
     if ring is not None:
         result["ring"] = ring
+    if comparator is not None:
+        result["comparator"] = comparator
     if subs:
         result["workloads"] = subs
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -462,7 +469,7 @@ def shrink(wl, args):
     return wl
 
 
-def measure_workload(name, tq, dev, stream, peak, store_reps=5, decode_reps=20):
+def measure_workload(name, tq, dev, stream, peak, store_reps=5, decode_reps=20, comparator=True):
     """Another configuration timed in the same run: its bulk store of every
     cached token and its decode of every sequence, device-resident inputs,
     CUDA events on the launch stream around each call.  K and V are drawn on
@@ -519,9 +526,59 @@ def measure_workload(name, tq, dev, stream, peak, store_reps=5, decode_reps=20):
         "inputs": "K/V drawn on the device with the configuration's distribution; caches and K/V larger than L2",
         "calls": {"store": store_reps, "decode": decode_reps},
     }
-    del k, v, cache, ws, out
+    del k, v
+    if comparator:
+        res["comparator"] = measure_comparator(tq, wl, cfg, cache, table, q, max_len, dev, stream, dt * 1e6)
+    del cache, ws, out
     torch.cuda.empty_cache()
     return res
+
+
+def measure_comparator(tq, wl, cfg, cache, table, q, max_len, dev, stream, fused_us, reps=5):
+    """The dequant-then-dense path ([ART] article, "Obstacle 1"), outside
+    the timed step: tq_dequant of every decode sequence's history to bf16 K
+    and V, then tq_dense_decode_attention over them; mean CUDA-event time of
+    each over `reps` calls, against the fused decode's time per call."""
+    import torch
+
+    lens = wl.seq_lens.astype(np.int64)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(dev)
+    n = int(lens.sum())
+    h, d = wl.num_kv_heads, wl.head_dim
+    k_rows = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
+    v_rows = torch.empty_like(k_rows)
+    ws = torch.zeros(tq.tq_dense_decode_workspace_size(d, wl.num_seqs, wl.num_q_heads, h, max_len),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((wl.num_seqs, wl.num_q_heads, d), dtype=torch.float32, device=dev)
+
+    def deq():
+        tq.tq_dequant(cfg, cache, table, cu, max_len, k_rows, v_rows, stream=stream)
+
+    def dense():
+        tq.tq_dense_decode_attention(q, k_rows, v_rows, cu, max_len, out, ws, stream=stream)
+
+    for _ in range(2):
+        deq()
+        dense()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, b, c in ev:
+        a.record(stream)
+        deq()
+        b.record(stream)
+        dense()
+        c.record(stream)
+    torch.cuda.synchronize()
+    dq_us = statistics.mean(a.elapsed_time(b) for a, b, _ in ev) * 1e3
+    dn_us = statistics.mean(b.elapsed_time(c) for _, b, c in ev) * 1e3
+    bf16_bytes = n * h * d * 2 * 2  # K and V rows, written by the dequant and read by the dense decode
+    del k_rows, v_rows, ws, out
+    torch.cuda.empty_cache()
+    return {"dequant_us": round(dq_us, 2), "dense_decode_us": round(dn_us, 2), "total_us": round(dq_us + dn_us, 2),
+            "fused_decode_us": round(fused_us, 2), "fused_speedup": round((dq_us + dn_us) / fused_us, 2),
+            "dense_decode_gbs_bf16": round(bf16_bytes / dn_us / 1e3, 1),
+            "note": "dequant of every decode sequence to bf16 K/V rows, then dense split-KV decode over them; "
+                    "not part of the timed step"}
 
 
 def measure_dequant(tq, wl, cfg, cache, table, max_len, dev, stream, peak, reps=10):
@@ -755,9 +812,6 @@ def run_e2e(args, tq, wl, cfg, caches, k_new, v_new, slots_new, q, table, lens, 
             "inputs": f"per step: new K and V uploaded once per layer ({len(caches)} uploads), slot ids, queries, "
                       "block table and lengths once; every layer's output read back"}
 
-
-#: seconds of untimed steps run under the clock sampler before the timed region
-PREROLL_S = 0.5
 
 #: GB300 L2 (129 MB): working sets that fit are flushed between timed kernels
 L2_BYTES = 129 * 1024 * 1024

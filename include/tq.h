@@ -337,6 +337,37 @@ TQ_API tq_status tq_hybrid_page(const tq_config* cfg, int32_t num_kv_heads, int3
                                 int64_t* page_bytes_out, int32_t* tokens_per_page_out);
 
 /*
+ * tq_dense_decode_workspace_size / tq_dense_decode_attention -- the
+ * comparison path of [ART] "Obstacle 1": attention over K and V that were
+ * first expanded to full precision (here bf16, by tq_dequant), instead of the
+ * fused decode over the packed cache.  For each sequence s and query head hq,
+ *     out[s, hq] = sum_t softmax_t(sm_scale * q[s,hq] . k_t) * v_t
+ * over rows t = cu_seqlens[s] .. cu_seqlens[s+1] - 1 of k and v, with query
+ * head hq reading KV head hq / (num_q_heads / num_kv_heads); products and
+ * sums in fp32, softmax by split-KV online softmax and a log-sum-exp merge.
+ *   q_dev: bf16 [num_seqs, num_q_heads, head_dim], 16-byte aligned
+ *   k_dev, v_dev: bf16 [cu_seqlens[num_seqs], num_kv_heads, head_dim] (the
+ *                 layout tq_dequant writes), 16-byte aligned
+ *   cu_seqlens_dev: int32 [num_seqs + 1]; every length <= max_seq_len
+ *   sm_scale: <= 0 selects 1/sqrt(head_dim)
+ *   out_dev: fp32 [num_seqs, num_q_heads, head_dim]
+ *   workspace_dev: >= tq_dense_decode_workspace_size(...) bytes, 16-byte
+ *                  aligned; every call writes all of it that it reads
+ * head_dim a power of two in [16, 256]; 1 to 8 query heads per KV head;
+ * num_seqs <= TQ_MAX_SEQS.  The workspace size depends on the device's SM
+ * count (the split count is chosen from it); query it on the device used.
+ * Asynchronous on `stream`; invalid arguments return before anything is
+ * enqueued.
+ */
+TQ_API size_t tq_dense_decode_workspace_size(int32_t head_dim, int32_t num_seqs, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t max_seq_len);
+TQ_API tq_status tq_dense_decode_attention(int32_t head_dim, const void* q_dev, int32_t num_seqs,
+                                           int32_t num_q_heads, int32_t num_kv_heads, const void* k_dev,
+                                           const void* v_dev, const int32_t* cu_seqlens_dev,
+                                           int32_t max_seq_len, float sm_scale, float* out_dev,
+                                           void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/*
  * tq_decode_attention_noalloc -- the same decode as tq_decode_attention, for
  * callers that cannot allocate device memory for its workspace.  The pages
  * have no counterpart: they do not discuss how decode scratch is allocated.

@@ -21,7 +21,7 @@ __all__ = [
     "tq_config_init", "tq_config_from_preset", "tq_layer_signs", "tq_store_kv",
     "tq_decode_workspace_size", "tq_decode_attention", "tq_decode_attention_noalloc", "tq_dequant",
     "tq_ring_workspace_size", "tq_ring_append", "tq_ring_step", "tq_decode_ring_workspace_size",
-    "tq_decode_attention_ring",
+    "tq_decode_attention_ring", "tq_dense_decode_workspace_size", "tq_dense_decode_attention",
     "new_ring", "tq_status_str", "TQ_NOALLOC_SCRATCH_BYTES", "TQ_RING_TOKENS", "TQ_MAX_SEQS",
     "new_paged_cache", "tq_hybrid_page", "PRESETS",
 ]
@@ -132,6 +132,12 @@ _SIGNATURES = {
                                                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                                 ctypes.c_void_p]),
+    "tq_dense_decode_workspace_size": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                         ctypes.c_int32, ctypes.c_int32]),
+    "tq_dense_decode_attention": (ctypes.c_int, [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_size_t, ctypes.c_void_p]),
     "tq_hybrid_page": (ctypes.c_int, [ctypes.POINTER(TqConfig), ctypes.c_int32, ctypes.c_int32,
                                       ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)]),
     "tq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
@@ -318,6 +324,33 @@ def tq_decode_attention_noalloc(cfg: TqConfig, q: torch.Tensor, cache: PagedCach
         _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
         _dev(seq_lens, torch.int32, "seq_lens"), int(max_seq_len), float(sm_scale), int(num_splits),
         _dev(out, torch.float32, "out"), _stream(stream)))
+
+
+# -- dequant-then-dense comparison path ([ART] article, "Obstacle 1") -------------------
+
+def tq_dense_decode_workspace_size(head_dim: int, num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                   max_seq_len: int) -> int:
+    n = lib().tq_dense_decode_workspace_size(head_dim, num_seqs, num_q_heads, num_kv_heads, max_seq_len)
+    if n == 0:
+        raise TQError(1, "invalid dense decode workspace query")
+    return int(n)
+
+
+def tq_dense_decode_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                              max_seq_len: int, out: torch.Tensor, workspace: torch.Tensor, sm_scale: float = 0.0,
+                              stream=None):
+    """Attention over bf16 K/V rows (the layout tq_dequant writes): q bf16
+    [S, Hq, d]; k, v bf16 [rows, H, d]; cu_seqlens int32 [S + 1]; out fp32
+    [S, Hq, d]; workspace uint8, tq_dense_decode_workspace_size bytes."""
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or k.shape[2] != q.shape[2] or out.shape != q.shape:
+        raise ValueError("q and out must be [S, Hq, d], k and v [rows, H, d]")
+    if cu_seqlens.shape != (q.shape[0] + 1,):
+        raise ValueError("cu_seqlens must be [num_seqs + 1]")
+    _check(lib().tq_dense_decode_attention(
+        q.shape[2], _dev(q, torch.bfloat16, "q"), q.shape[0], q.shape[1], k.shape[1], _dev(k, torch.bfloat16, "k"),
+        _dev(v, torch.bfloat16, "v"), _dev(cu_seqlens, torch.int32, "cu_seqlens"), int(max_seq_len),
+        float(sm_scale), _dev(out, torch.float32, "out"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream(stream)))
 
 
 # -- ring-buffered store ([ART] article, full_tq write path) ------------------------

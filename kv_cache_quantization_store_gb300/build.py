@@ -24,7 +24,7 @@ LIB = PKG / "libtq.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = [
     "tq_host.cpp", "tq_store.cu", "tq_decode.cu", "tq_decode_mma.cu", "tq_decode_mma_d64.cu",
-    "tq_decode_mma_d128.cu", "tq_decode_mma_d256.cu", "tq_dequant.cu", "tq_noalloc.cu",
+    "tq_decode_mma_d128.cu", "tq_decode_mma_d256.cu", "tq_dequant.cu", "tq_noalloc.cu", "tq_dense.cu",
 ]
 
 

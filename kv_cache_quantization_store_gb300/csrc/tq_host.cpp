@@ -494,6 +494,53 @@ tq_status tq_dequant(const tq_config* cfg, const tq_cache* cache, const int32_t*
     return TQ_OK;
 }
 
+size_t tq_dense_decode_workspace_size(int32_t head_dim, int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t max_seq_len) {
+    if (!tq::supported_head_dim(head_dim) || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        max_seq_len < 0)
+        return 0;
+    int sms = 1;
+    if (sm_count(&sms) != TQ_OK) return 0;
+    return tq::plan_dense(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, sms).workspace_bytes;
+}
+
+tq_status tq_dense_decode_attention(int32_t head_dim, const void* q_dev, int32_t num_seqs, int32_t num_q_heads,
+                                    int32_t num_kv_heads, const void* k_dev, const void* v_dev,
+                                    const int32_t* cu_seqlens_dev, int32_t max_seq_len, float sm_scale,
+                                    float* out_dev, void* workspace_dev, size_t workspace_bytes, void* stream) {
+    if (!tq::supported_head_dim(head_dim))
+        return fail(TQ_ERR_UNSUPPORTED, "head_dim %d is not a power of two in [16, 256]", head_dim);
+    if (num_seqs < 0 || max_seq_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
+        return fail(TQ_ERR_INVALID_ARG, "negative size argument");
+    if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 8)
+        return fail(TQ_ERR_UNSUPPORTED, "num_q_heads (%d) must be 1 to 8 times num_kv_heads (%d)", num_q_heads,
+                    num_kv_heads);
+    if (num_seqs > TQ_MAX_SEQS)
+        return fail(TQ_ERR_UNSUPPORTED, "num_seqs (%d) above %d (one grid row per sequence)", num_seqs, TQ_MAX_SEQS);
+    if (num_kv_heads > 65535) return fail(TQ_ERR_UNSUPPORTED, "num_kv_heads above 65535");
+    if (num_seqs == 0) return TQ_OK;
+    if (q_dev == nullptr || k_dev == nullptr || v_dev == nullptr || cu_seqlens_dev == nullptr || out_dev == nullptr)
+        return fail(TQ_ERR_INVALID_ARG, "q, k, v, cu_seqlens and out must not be NULL");
+    if (!aligned(q_dev, 16) || !aligned(k_dev, 16) || !aligned(v_dev, 16) || !aligned(out_dev, 4) ||
+        !aligned(cu_seqlens_dev, 4))
+        return fail(TQ_ERR_INVALID_ARG, "q, k and v must be 16-byte aligned, out and cu_seqlens 4-byte aligned");
+    int sms = 1;
+    tq_status st = sm_count(&sms);
+    if (st != TQ_OK) return st;
+    const tq::DensePlan plan = tq::plan_dense(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, sms);
+    if (workspace_dev == nullptr || workspace_bytes < plan.workspace_bytes)
+        return fail(TQ_ERR_WORKSPACE, "dense decode workspace needs %zu bytes (got %zu)", plan.workspace_bytes,
+                    workspace_bytes);
+    if (!aligned(workspace_dev, 16)) return fail(TQ_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+    const cudaError_t e = tq::launch_dense_decode(
+        head_dim, static_cast<const uint16_t*>(q_dev), num_seqs, num_q_heads, num_kv_heads,
+        static_cast<const uint16_t*>(k_dev), static_cast<const uint16_t*>(v_dev), cu_seqlens_dev, max_seq_len, scale,
+        plan, out_dev, workspace_dev, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tq_dense_decode_attention launch");
+    return TQ_OK;
+}
+
 tq_status tq_hybrid_page(const tq_config* cfg, int32_t num_kv_heads, int32_t skip_dtype_bytes,
                          int64_t* page_bytes_out, int32_t* tokens_per_page_out) {
     tq::LayerParams lp;

@@ -107,6 +107,18 @@ cudaError_t launch_dequant(const LayerParams& p, const CacheGeom& c, const int32
                            int max_blocks_per_seq, const int32_t* cu_seqlens, int num_seqs,
                            int max_seq_len, uint16_t* k_out, uint16_t* v_out, int sm_count, cudaStream_t stream);
 
+// Dense decode over bf16 K/V rows (the dequant-then-attend comparison path).
+struct DensePlan {
+    int32_t num_splits;
+    int32_t tokens_per_split;
+    size_t workspace_bytes;
+};
+DensePlan plan_dense(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_seq_len, int sm_count);
+cudaError_t launch_dense_decode(int head_dim, const uint16_t* q, int num_seqs, int num_q_heads, int num_kv_heads,
+                                const uint16_t* k, const uint16_t* v, const int32_t* cu_seqlens, int max_seq_len,
+                                float sm_scale, const DensePlan& plan, float* out, void* workspace,
+                                cudaStream_t stream);
+
 // Records the text tq_last_error() returns on this host thread.
 void set_last_error(const char* msg);
 
