@@ -66,6 +66,45 @@ __device__ __forceinline__ void fwht_lanes_fma(float (&x)[N], int part) {
     }
 }
 
+// The same transforms on float2 pairs (x[m] = elements 2m, 2m + 1), with
+// Blackwell's packed FADD2 / FFMA2 doing two butterflies per instruction
+// from the second stage on; each element is still rounded once per stage,
+// so the results equal the scalar versions bit for bit.
+template <int N2>
+__device__ __forceinline__ void fwht_local2(float2 (&x)[N2]) {
+#pragma unroll
+    for (int m = 0; m < N2; ++m) {
+        const float a = x[m].x, b = x[m].y;
+        x[m] = make_float2(a + b, a - b);
+    }
+    const float2 neg1 = make_float2(-1.f, -1.f);
+#pragma unroll
+    for (int s = 1; s < N2; s <<= 1) {
+#pragma unroll
+        for (int m = 0; m < N2; ++m) {
+            if ((m & s) == 0) {
+                const float2 a = x[m], b = x[m + s];
+                x[m] = __fadd2_rn(a, b);
+                x[m + s] = __ffma2_rn(b, neg1, a);
+            }
+        }
+    }
+}
+
+template <int N2, int LPV>
+__device__ __forceinline__ void fwht_lanes2(float2 (&x)[N2], int part) {
+#pragma unroll
+    for (int m = 1; m < LPV; m <<= 1) {
+        const float sg = (part & m) ? -1.f : 1.f;
+        const float2 sg2 = make_float2(sg, sg);
+#pragma unroll
+        for (int i = 0; i < N2; ++i) {
+            const float2 o = make_float2(__shfl_xor_sync(kFull, x[i].x, m), __shfl_xor_sync(kFull, x[i].y, m));
+            x[i] = __ffma2_rn(sg2, x[i], o);
+        }
+    }
+}
+
 template <int LPV>
 __device__ __forceinline__ float sum_lanes(float v) {
 #pragma unroll

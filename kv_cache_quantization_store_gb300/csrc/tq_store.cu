@@ -20,22 +20,33 @@ namespace {
 
 constexpr int kStoreWarps = 8;
 
-// Number of the positive decision thresholds t[0] < t[1] < ... below a >= 0
-// (strictly), by binary search over the 3 (3-bit) or 7 (4-bit) thresholds.
-template <int NT>
-__device__ __forceinline__ uint32_t count_above(float a, const float (&t)[NT]) {
-    static_assert(NT == 3 || NT == 7, "3 or 7 positive thresholds");
-    if constexpr (NT == 3) {
-        const bool p1 = a > t[1];
-        const bool p2 = a > (p1 ? t[2] : t[0]);
-        return (p1 ? 2u : 0u) + (p2 ? 1u : 0u);
-    } else {
-        const bool p1 = a > t[3];
-        const bool p2 = a > (p1 ? t[5] : t[1]);
-        const float tc = p1 ? (p2 ? t[6] : t[4]) : (p2 ? t[2] : t[0]);
-        const bool p3 = a > tc;
-        return (p1 ? 4u : 0u) + (p2 ? 2u : 0u) + (p3 ? 1u : 0u);
-    }
+// Key index by table lookup.  A monotone map of the unit-vector coordinate
+// y in [-1, 1] onto 256 buckets, g(y) = RN(127 y + 128 + 1.5 * 2^23) & 0xFF
+// (one fma; the 1.5 * 2^23 puts the rounded integer in the low mantissa
+// bits), is applied to the boundaries and to every coordinate alike.
+// Because g is non-decreasing, a boundary whose bucket is below g(y) lies
+// below y, and one whose bucket is above lies above; so with at most one
+// boundary per bucket (the Lloyd-Max boundaries are at least 0.25 sigma
+// apart, two or more buckets at d <= 256) the count of boundaries strictly
+// below y is base[g(y)] + (y > thr[g(y)]), where base[b] counts the
+// boundaries in buckets below b and thr[b] is the boundary in bucket b
+// (+inf if none).  The table is built on the device from the fp32
+// boundaries with the same fma, so both sides round alike.
+//
+// An entry is one 32-bit word: the threshold's fp32 bits with base in the
+// low 4 mantissa bits.  Compared as a float, that word differs from the
+// threshold by at most 15 ulp (3.6e-6 relative; a tiny subnormal for the
+// boundary at 0; a NaN, which compares false like +inf, for no boundary),
+// so a key index can change only for coordinates that close to a
+// boundary, inside the near-boundary window where the stored index is not
+// pinned to the oracle's.  One word per lookup keeps the table at 1 KB and
+// its reads at one 4-byte load.
+constexpr int kBuckets = 256;
+constexpr float kBucketScale = 127.f;
+constexpr float kBucketMagic = 12583040.f;  // 128 + 1.5 * 2^23
+
+__device__ __forceinline__ uint32_t bucket_of(float y) {
+    return __float_as_uint(__fmaf_rn(y, kBucketScale, kBucketMagic)) & (kBuckets - 1);
 }
 
 // Correctly rounded fp32 quotient a / s from y = RN(1 / s): q0 = RN(a y) is
@@ -144,6 +155,8 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     // K and V rows of the warp's next step, prefetched by bulk copies
     extern __shared__ __align__(16) uint8_t kv_ring[];  // [warp][slot][K | V][kSpan] bf16
     __shared__ __align__(8) uint64_t kv_full[kStoreWarps][2];
+    // key-index buckets: {threshold bits, boundaries below the bucket}
+    __shared__ uint32_t bucket_tab[KB == 8 ? 1 : kBuckets];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -159,10 +172,18 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
     }
     const int64_t num_vecs = num_tokens * H;
 
-    // Sign masks, and the positive-half decision thresholds (the grid is
-    // symmetric about 0 and the middle boundary is 0).
-    float pos_b[kHalf - 1];
+    // Sign masks and the bucket table of the decision boundaries.
     if constexpr (KB != 8) {
+        for (int bk = threadIdx.x; bk < kBuckets; bk += kStoreWarps * 32) {
+            uint32_t thr = 0x7F800000u, below = 0;  // +inf: no boundary in this bucket
+#pragma unroll
+            for (int j = 0; j < 2 * kHalf - 1; ++j) {
+                const uint32_t bj = bucket_of(p.boundaries[j]);
+                below += bj < static_cast<uint32_t>(bk) ? 1u : 0u;
+                if (bj == static_cast<uint32_t>(bk)) thr = __float_as_uint(p.boundaries[j]);
+            }
+            bucket_tab[bk] = (thr & ~0xFu) | below;
+        }
         for (int i = threadIdx.x; i < LPV * EPL / 2; i += kStoreWarps * 32) {
             const int pp = i / (EPL / 2), jw = i % (EPL / 2);
             const int e = 8 * (pp + LPV * (jw / 4)) + 2 * (jw % 4);
@@ -170,8 +191,6 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
             const uint32_t b1 = (p.sign_mask[(e + 1) / 32] >> ((e + 1) % 32)) & 1u;
             sign_mask[pp][jw] = (b0 << 15) | (b1 << 31);
         }
-#pragma unroll
-        for (int j = 0; j < kHalf - 1; ++j) pos_b[j] = p.boundaries[kHalf + j];
     }
     if (kPrefetch && threadIdx.x == 0) {
         for (int w = 0; w < kStoreWarps; ++w) {
@@ -313,6 +332,7 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                 }
             } else {
                 // bf16 pairs with the random signs applied to the raw sign bits
+                float2 x2[EPL / 2];
                 const uint4* msk = reinterpret_cast<const uint4*>(sign_mask[part]);
 #pragma unroll
                 for (int j = 0; j < EPL / 8; ++j) {
@@ -320,32 +340,33 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
                     const uint4 m = msk[j];
                     const uint32_t w[4] = {u.x ^ m.x, u.y ^ m.y, u.z ^ m.z, u.w ^ m.w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        x[8 * j + 2 * q] = bf16_lo(w[q]);
-                        x[8 * j + 2 * q + 1] = bf16_hi(w[q]);
-                    }
+                    for (int q = 0; q < 4; ++q) x2[4 * j + q] = make_float2(bf16_lo(w[q]), bf16_hi(w[q]));
                 }
-                float ss = 0.f;  // the signs do not change the squares
+                float2 ss2 = make_float2(0.f, 0.f);  // the signs do not change the squares
 #pragma unroll
-                for (int i = 0; i < EPL; ++i) ss = fmaf(x[i], x[i], ss);
-                ss = sum_lanes<LPV>(ss);
+                for (int i = 0; i < EPL / 2; ++i) ss2 = __ffma2_rn(x2[i], x2[i], ss2);
+                const float ss = sum_lanes<LPV>(ss2.x + ss2.y);
                 const float n = sqrtf(ss);
-                fwht_local<EPL>(x);
-                fwht_lanes_fma<EPL, LPV>(x, part);
-                // x = sqrt(d) * n * y with y = Pi k / n; compare against the
-                // boundaries scaled the same way.
-                const float u = n * sqrt_d;
-                float t[kHalf - 1];
-#pragma unroll
-                for (int j = 0; j < kHalf - 1; ++j) t[j] = pos_b[j] * u;
+                fwht_local2<EPL / 2>(x2);
+                fwht_lanes2<EPL / 2, LPV>(x2, part);
+                // x = sqrt(d) n y with y = Pi k / n: y = x / (n sqrt(d)), then the
+                // bucket table (a zero key gives y = 0, the lower middle cell)
+                const float un = n * sqrt_d;
+                const float inv_u = un > 0.f ? __frcp_rn(un) : 0.f;
+                const float2 inv2 = make_float2(inv_u, inv_u);
+                const float2 sc2 = make_float2(kBucketScale, kBucketScale);
+                const float2 mg2 = make_float2(kBucketMagic, kBucketMagic);
 #pragma unroll
                 for (int j = 0; j < EPL / 8; ++j) {
                     uint32_t code[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float xe = x[8 * j + e];
-                        const uint32_t cnt = count_above(fabsf(xe), t);
-                        code[e] = xe > 0.f ? kHalf + cnt : kHalf - 1 - cnt;
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 y2 = __fmul2_rn(x2[4 * j + e], inv2);
+                        const float2 g2 = __ffma2_rn(y2, sc2, mg2);
+                        const uint32_t t0 = bucket_tab[__float_as_uint(g2.x) & (kBuckets - 1)];
+                        const uint32_t t1 = bucket_tab[__float_as_uint(g2.y) & (kBuckets - 1)];
+                        code[2 * e] = (t0 & 0xFu) + (y2.x > __uint_as_float(t0) ? 1u : 0u);
+                        code[2 * e + 1] = (t1 & 0xFu) + (y2.y > __uint_as_float(t1) ? 1u : 0u);
                     }
                     put_bytes<KB>(my_slot + KB * (part + LPV * j), pack8<KB>(code), false);
                 }
@@ -356,22 +377,19 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
 
         // ---- value ---------------------------------------------------------
         {
-            float x[EPL];
+            float2 x2[EPL / 2];
 #pragma unroll
             for (int j = 0; j < EPL / 8; ++j) {
                 const uint4 u = ld16(vsrc, j);
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    x[8 * j + 2 * q] = bf16_lo(w[q]);
-                    x[8 * j + 2 * q + 1] = bf16_hi(w[q]);
-                }
+                for (int q = 0; q < 4; ++q) x2[4 * j + q] = make_float2(bf16_lo(w[q]), bf16_hi(w[q]));
             }
-            float mn = x[0], mx = x[0];
+            float mn = fminf(x2[0].x, x2[0].y), mx = fmaxf(x2[0].x, x2[0].y);
 #pragma unroll
-            for (int i = 1; i < EPL; ++i) {
-                mn = fminf(mn, x[i]);
-                mx = fmaxf(mx, x[i]);
+            for (int i = 1; i < EPL / 2; ++i) {
+                mn = fminf(mn, fminf(x2[i].x, x2[i].y));
+                mx = fmaxf(mx, fmaxf(x2[i].x, x2[i].y));
             }
             mn = min_lanes<LPV>(mn);
             mx = max_lanes<LPV>(mx);
@@ -381,19 +399,42 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
             const float z = half_from_bits(zb);
             uint32_t code[EPL];
             if (isfinite(mn) && isfinite(mx) && isfinite(z) && isfinite(s)) {
-                // y = 0 for a zero scale gives quotient 0, i.e. code 0
+                // y = 0 for a zero scale gives quotient 0, i.e. code 0.  Two
+                // elements per packed op; each keeps its own rounding: RN(v - z),
+                // then the correctly rounded quotient (see quotient_rn).
                 const float y = (s == 0.f) ? 0.f : __frcp_rn(s);
+                const float2 y2 = make_float2(y, y), ns2 = make_float2(-s, -s), nz2 = make_float2(-z, -z);
+                const float2 magic2 = make_float2(12582912.f, 12582912.f);
+                if constexpr (KB == 8) {
+                    // FP8 keys leave the store bound by memory, where the
+                    // scalar form measured faster than the packed one
 #pragma unroll
-                for (int i = 0; i < EPL; ++i) {
-                    const float qv = quotient_rn(__fsub_rn(x[i], z), s, y);
+                    for (int i = 0; i < EPL; ++i) {
+                        const float xi = (i & 1) ? x2[i / 2].y : x2[i / 2].x;
+                        const float qv = quotient_rn(__fsub_rn(xi, z), s, y);
+                        const float cl = fminf(fmaxf(qv, 0.f), static_cast<float>(kTopV));
+                        code[i] = __float_as_uint(__fadd_rn(cl, 12582912.f)) & static_cast<uint32_t>(kTopV);
+                    }
+                } else {
+#pragma unroll
+                for (int i = 0; i < EPL / 2; ++i) {
+                    const float2 a2 = __fadd2_rn(x2[i], nz2);
+                    const float2 q0 = __fmul2_rn(a2, y2);
+                    const float2 r2 = __ffma2_rn(ns2, q0, a2);
+                    const float2 qv = __ffma2_rn(r2, y2, q0);
                     // clamp, then round half to even by the 1.5 * 2^23 addition
-                    const float cl = fminf(fmaxf(qv, 0.f), static_cast<float>(kTopV));
-                    code[i] = __float_as_uint(__fadd_rn(cl, 12582912.f)) & static_cast<uint32_t>(kTopV);
+                    const float2 cl = make_float2(fminf(fmaxf(qv.x, 0.f), static_cast<float>(kTopV)),
+                                                  fminf(fmaxf(qv.y, 0.f), static_cast<float>(kTopV)));
+                    const float2 rr = __fadd2_rn(cl, magic2);
+                    code[2 * i] = __float_as_uint(rr.x) & static_cast<uint32_t>(kTopV);
+                    code[2 * i + 1] = __float_as_uint(rr.y) & static_cast<uint32_t>(kTopV);
+                }
                 }
             } else {
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) {
-                    const float qv = __fdiv_rn(__fsub_rn(x[i], z), s);
+                    const float xi = (i & 1) ? x2[i / 2].y : x2[i / 2].x;
+                    const float qv = __fdiv_rn(__fsub_rn(xi, z), s);
                     const float r = fminf(fmaxf(rintf(qv), 0.f), static_cast<float>(kTopV));
                     code[i] = (s == 0.f) ? 0u : static_cast<uint32_t>(r);
                 }

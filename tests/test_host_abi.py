@@ -302,3 +302,21 @@ def test_binding_checks_row_shapes(libtq):
     with pytest.raises(ValueError, match="ring_k"):
         tq.tq_decode_attention_ring(cfg, q, cache, table, lens, 16, ring_bad, ring_bad, out,
                                     torch.zeros(64, dtype=torch.uint8))
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("bits", [3, 4])
+def test_store_bucket_table_has_one_boundary_per_bucket(libtq, d, bits):
+    """The store finds a key index through 256 buckets g(y) = RN(127 y + 128 +
+    1.5 * 2^23) & 0xFF of the unit-vector coordinate (one fma, tq_store.cu);
+    its table holds one boundary per bucket, so every supported codebook's
+    fp32 boundaries must fall in distinct buckets, in order."""
+    import kv_cache_quantization_store_gb300 as tq
+
+    cfg = tq.tq_config_init(d, bits, 4, False)
+    b = np.array(cfg.boundary_list(), dtype=np.float32).astype(np.float64)
+    # the fma: exact product and sum in fp64, one rounding to fp32
+    g = (b * 127.0 + 12583040.0).astype(np.float32).view(np.uint32) & 0xFF
+    assert len(set(g.tolist())) == len(g)
+    assert np.all(np.diff(g.astype(np.int64)) > 0)
+    assert g.min() >= 1 and g.max() <= 254  # |y| <= 1 maps into [1, 255]
