@@ -26,9 +26,11 @@
 //   QK   S[16 tok x 8 cols] = Khat[16 x d] * Q'^T[d x 8]
 //        Thread (r = lane/4, c = lane%4) feeds key dims of tokens r and
 //        r+8; each A register is one pair of consecutive dims, looked up
-//        from a per-lane-replicated pair table of half2 centroids in shared
-//        memory (3-bit: 64 entries, 4-bit: 256), or converted from two FP8
-//        bytes.  Q' is permuted to the same dim order and split into fp16 hi
+//        from a pair table of half2 centroids in shared memory (3-bit: 64
+//        entries, 4-bit: 256), or converted from two FP8 bytes.  The table
+//        has one copy per lane (32), or 16 copies shared by lanes l and
+//        l + 16 when three CTAs share an SM (a 4-bit table of 32 KB would not
+//        fit three times).  Q' is permuted to the same dim order and split into fp16 hi
 //        + lo parts: with G <= 4 columns 0-3 carry the hi and 4-7 the lo
 //        parts (one MMA and a shuffle), else two MMAs.  The table holds the
 //        centroids times a scale chosen so that their fp16 rounding error is
@@ -196,7 +198,7 @@ __device__ __forceinline__ constexpr float value_weight(int n) {
 
 // Compile-time geometry of one kernel instantiation.  Shared memory:
 // [pair table][score exchange x2][control][16 zero bytes][stage ring][Q' fragments].
-template <int D, int KB, int VB, int H, int WPH, int NS, bool PACKQ>
+template <int D, int KB, int VB, int H, int WPH, int NS, bool PACKQ, int LREP = 32>
 struct Geo {
     using S = Slot<D, KB, VB>;
     static constexpr int SA = S::kAligned;
@@ -227,7 +229,9 @@ struct Geo {
     static constexpr int VNU = VSH / (8 * VUNIT);   // value units of one lane and token
     static constexpr int VREGS = VUNITS ? VNU : VWORDS;
     static constexpr int LUT_ENTRIES = KB == 3 ? 64 : (KB == 4 ? 256 : 0);
-    static constexpr int LUT_BYTES = LUT_ENTRIES * 32 * 4;  // half2 per entry and lane
+    static constexpr int LUT_REP = LREP;                    // copies of the table (lanes l and l + LREP share one)
+    static constexpr int LUT_SHIFT = LREP == 32 ? 7 : 6;    // log2 of an entry's stride (LREP x 4 bytes)
+    static constexpr int LUT_BYTES = LUT_ENTRIES * LREP * 4;  // half2 per entry and copy
     static constexpr int XCH_W = WPH > 1 ? 32 * 6 * 4 : 0;  // per warp and buffer: 32 x {4 scores, 2 norms}
     static constexpr int X_OFF = LUT_BYTES;
     // control block: full mbarrier, release counter, block id per stage; error word
@@ -254,7 +258,7 @@ struct Geo {
 template <int D, int KB, int VB, bool NC, int H, int WPH, int NS, int MINB, bool PACKQ>
 __global__ void __launch_bounds__(32 * H * WPH, MINB)
 decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
-    using G = Geo<D, KB, VB, H, WPH, NS, PACKQ>;
+    using G = Geo<D, KB, VB, H, WPH, NS, PACKQ, (MINB >= 3 ? 16 : 32)>;
     using S = typename G::S;
     static_assert(((D / 4 / WPH) * KB) % 8 == 0 && ((D / 8 / WPH) * VB) % 8 == 0,
                   "a warp's share of the codes must start on a byte");
@@ -354,14 +358,14 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         for (int it = 0; it < early && it < nch; ++it) issue(it);
     }
 
-    // ---- pair lookup table: centroids * lut_scale as fp16, one copy per lane ----
+    // ---- pair lookup table: centroids * lut_scale as fp16 (lane l reads copy l % LUT_REP) --
     const float ls = a.lut_scale;
     if constexpr (KB == 3 || KB == 4) {
-        // entry e = codes (e & mask, e >> bits) of a dim pair, 32 lanes x 4 bytes;
+        // entry e = codes (e & mask, e >> bits) of a dim pair, LUT_REP copies x 4 bytes;
         // one 16-byte store writes four lanes' copies
         constexpr int kBits = KB, kMask = (1 << KB) - 1;
-        for (int i = threadIdx.x; i < G::LUT_ENTRIES * 8; i += NT) {
-            const int e = i >> 3;
+        for (int i = threadIdx.x; i < G::LUT_ENTRIES * (G::LUT_REP / 4); i += NT) {
+            const int e = i / (G::LUT_REP / 4);
             const uint32_t hv = pack_half2(p.centroids[e & kMask] * ls, p.centroids[e >> kBits] * ls);
             reinterpret_cast<uint4*>(smem)[i] = make_uint4(hv, hv, hv, hv);
         }
@@ -500,7 +504,7 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     const int v_off0 = sig(2 * cc) * ROW + vbase, v_off1 = sig(2 * cc + 1) * ROW + vbase;
     const int v_off8 = sig(2 * cc + 8) * ROW + vbase, v_off9 = sig(2 * cc + 9) * ROW + vbase;
     const uint8_t* lut = smem;
-    const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
+    const uint32_t lane4 = static_cast<uint32_t>(lane & (G::LUT_REP - 1)) << 2;
     float* xch = reinterpret_cast<float*>(smem + G::X_OFF);  // [buffer][warp][32 float4 | 32 float2]
 
     // ---- QK of one staged chunk: log2-domain scores of tokens r, r + 8 for
@@ -535,24 +539,27 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
                 e4m3x4_to_f16x2(kw1[j], af[1], af[3]);
             } else if constexpr (KB == 4) {
                 // unit j: two pair codes, one per byte, moved to bit 7 (table rows of 128 bytes)
-                af[0] = ld32(lut + (((kw0[j] << 7) & 0x7F80u) | lane4));
-                af[1] = ld32(lut + (((kw1[j] << 7) & 0x7F80u) | lane4));
-                af[2] = ld32(lut + (((kw0[j] >> 1) & 0x7F80u) | lane4));
-                af[3] = ld32(lut + (((kw1[j] >> 1) & 0x7F80u) | lane4));
+                constexpr int kS = G::LUT_SHIFT;
+                constexpr uint32_t kM = 0xFFu << kS;
+                af[0] = ld32(lut + (((kw0[j] << kS) & kM) | lane4));
+                af[1] = ld32(lut + (((kw1[j] << kS) & kM) | lane4));
+                af[2] = ld32(lut + (((kw0[j] >> (8 - kS)) & kM) | lane4));
+                af[3] = ld32(lut + (((kw1[j] >> (8 - kS)) & kM) | lane4));
             } else {
                 // 6-bit pair codes at bit 6 * pair of the lane's block, moved to bit 7
-                constexpr uint32_t kIdx = 0x3Fu << 7;
+                constexpr int kS = G::LUT_SHIFT;
+                constexpr uint32_t kIdx = 0x3Fu << kS;
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int bit = 6 * (2 * j + e);
                     const int wi = bit / 32, off = bit % 32;
                     uint32_t x0, x1;
                     if (off + 6 <= 32) {
-                        x0 = off <= 7 ? (kw0[wi] << (7 - off)) : (kw0[wi] >> (off - 7));
-                        x1 = off <= 7 ? (kw1[wi] << (7 - off)) : (kw1[wi] >> (off - 7));
+                        x0 = off <= kS ? (kw0[wi] << (kS - off)) : (kw0[wi] >> (off - kS));
+                        x1 = off <= kS ? (kw1[wi] << (kS - off)) : (kw1[wi] >> (off - kS));
                     } else {
-                        x0 = __funnelshift_r(kw0[wi], kw0[wi + 1], off - 7);
-                        x1 = __funnelshift_r(kw1[wi], kw1[wi + 1], off - 7);
+                        x0 = __funnelshift_r(kw0[wi], kw0[wi + 1], off - kS);
+                        x1 = __funnelshift_r(kw1[wi], kw1[wi + 1], off - kS);
                     }
                     af[2 * e] = ld32(lut + ((x0 & kIdx) | lane4));
                     af[2 * e + 1] = ld32(lut + ((x1 & kIdx) | lane4));
@@ -923,16 +930,23 @@ constexpr int pick_wph(int want) {
 
 // Launch policy per shape: warps per head, resident CTAs per SM aimed for,
 // and the deepest stage ring that fits the shared memory that leaves.
+// About four warps per CTA: with up to four KV heads each warp takes a whole
+// head (no split dims, so no score exchange and no duplicated softmax) and
+// three CTAs share an SM (registers allow ~170 per thread; shared memory
+// then takes the 16-copy table and a 2-stage ring).  At d = 256, 4 KV heads
+// this measured 173.6 us per decode of 256 x 2048 tokens against 190.7 us
+// with two warps per head and two CTAs per SM.  Eight KV heads keep one warp
+// per head in 256-thread CTAs, two per SM.
 template <int D, int KB, int VB, int H, bool PACKQ>
 struct Policy {
-    static constexpr int kWarpsTarget = 8;
+    static constexpr int kWarpsTarget = 4;
     static constexpr int kWphRaw = kWarpsTarget / H;
     static constexpr int kWphMax = D / 32;  // at least two k-steps per warp
     static constexpr int WPH = pick_wph<D, KB, VB>(kWphRaw < 1 ? 1 : (kWphRaw > kWphMax ? kWphMax : kWphRaw));
-    static constexpr int MINB = 32 * H * WPH > 256 ? 1 : 2;
+    static constexpr int MINB = 32 * H * WPH > 256 ? 1 : (32 * H * WPH > 128 ? 2 : 3);
     // per-CTA shared memory: 228 KB per SM, less 1 KB reserved per CTA
-    static constexpr int kBudget = MINB == 1 ? 227 * 1024 : 113 * 1024;
-    using G1 = Geo<D, KB, VB, H, WPH, 8, PACKQ>;
+    static constexpr int kBudget = MINB == 1 ? 227 * 1024 : (MINB == 2 ? 113 * 1024 : 74 * 1024);
+    using G1 = Geo<D, KB, VB, H, WPH, 8, PACKQ, (MINB >= 3 ? 16 : 32)>;
     // fixed part plus the query fragments (unpacked: up to 5 query heads per KV head)
     static constexpr int kFixed = G1::RING_OFF + 16 + (PACKQ ? H * D * 16 : H * 5 * D * 4);
     static constexpr int kNs = (kBudget - kFixed) / G1::STAGE;
@@ -1001,7 +1015,7 @@ int load_wavefronts(bool eo) {
 template <int D, int KB, int VB, bool NC, int H, bool PACKQ>
 struct Kernel {
     using P = Policy<D, KB, VB, H, PACKQ>;
-    using G = Geo<D, KB, VB, H, P::WPH, P::NS, PACKQ>;
+    using G = Geo<D, KB, VB, H, P::WPH, P::NS, PACKQ, (P::MINB >= 3 ? 16 : 32)>;
     static constexpr auto fn = decode_kernel<D, KB, VB, NC, H, P::WPH, P::NS, P::MINB, PACKQ>;
 
     // Per device (function attributes belong to a device's context): the

@@ -65,6 +65,76 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w) {
     return r;
 }
 
+// One (token, head) vector: this lane's EPL elements of the key and the value
+// read from `slot` (global or shared memory) and written as bf16 to kdst /
+// vdst (16-byte groups LPV apart) when `ok`.
+template <int D, int KB, int VB>
+__device__ __forceinline__ void dequant_vector(const uint8_t* slot, bool ok, uint4* kdst, uint4* vdst, int part,
+                                               const float* cent, const uint32_t* sign_mask_part, bool nc,
+                                               float inv_sqrt_d) {
+    using S = Slot<D, KB, VB>;
+    using LS = LaneSplit<D>;
+    constexpr int EPL = LS::kEPL, LPV = LS::kLPV;
+    // ---- key -----------------------------------------------------------
+    if constexpr (KB == 8) {
+#pragma unroll
+        for (int j = 0; j < EPL / 8; ++j) {
+            const uint64_t b = get_bytes<8>(slot + 8 * (part + LPV * j));
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = e4m3x2_to_bf16x2(static_cast<uint32_t>(b >> (16 * q)));
+            if (ok) kdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        float x[EPL];
+        float nsq = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPL / 8; ++j) {
+            const uint64_t b = get_bytes<KB>(slot + KB * (part + LPV * j));
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                x[8 * j + e] = cent[static_cast<uint32_t>(b >> (KB * e)) & ((1u << KB) - 1u)];
+                nsq = fmaf(x[8 * j + e], x[8 * j + e], nsq);
+            }
+        }
+        nsq = sum_lanes<LPV>(nsq);
+        const float vec_norm = half_from_bits(*reinterpret_cast<const uint16_t*>(slot + S::kKeyIdxBytes));
+        float f = vec_norm * inv_sqrt_d;
+        if (nc) f = f / sqrtf(nsq);
+        fwht_local<EPL>(x);
+        fwht_lanes_fma<EPL, LPV>(x, part);
+        const uint4* msk = reinterpret_cast<const uint4*>(sign_mask_part);
+#pragma unroll
+        for (int j = 0; j < EPL / 8; ++j) {
+            const uint4 m = msk[j];
+            const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = bf16_pair(x[8 * j + 2 * q] * f, x[8 * j + 2 * q + 1] * f) ^ mw[q];
+            if (ok) kdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+
+    // ---- value ---------------------------------------------------------
+    {
+        const uint16_t* sz = reinterpret_cast<const uint16_t*>(slot + S::kKeyBytes + S::kValCodeBytes);
+        const float sc = half_from_bits(sz[0]);
+        const float z = half_from_bits(sz[1]);
+#pragma unroll
+        for (int j = 0; j < EPL / 8; ++j) {
+            const uint64_t b = get_bytes<VB>(slot + S::kKeyBytes + VB * (part + LPV * j));
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float c0 = static_cast<float>(static_cast<uint32_t>(b >> (VB * 2 * q)) & ((1u << VB) - 1u));
+                const float c1 = static_cast<float>(static_cast<uint32_t>(b >> (VB * (2 * q + 1))) & ((1u << VB) - 1u));
+                w[q] = bf16_pair(fmaf(sc, c0, z), fmaf(sc, c1, z));
+            }
+            if (ok) vdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(kDqWarps * 32)
 dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict__ block_table,
@@ -125,64 +195,125 @@ dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict
         uint4* kdst = reinterpret_cast<uint4*>(k_out + ((row0 + pos) * H + h) * D) + part;
         uint4* vdst = reinterpret_cast<uint4*>(v_out + ((row0 + pos) * H + h) * D) + part;
 
-        // ---- key -----------------------------------------------------------
-        if constexpr (KB == 8) {
-#pragma unroll
-            for (int j = 0; j < EPL / 8; ++j) {
-                const uint64_t b = get_bytes<8>(slot + 8 * (part + LPV * j));
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) w[q] = e4m3x2_to_bf16x2(static_cast<uint32_t>(b >> (16 * q)));
-                if (ok) kdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        } else {
-            float x[EPL];
-            float nsq = 0.f;
-#pragma unroll
-            for (int j = 0; j < EPL / 8; ++j) {
-                const uint64_t b = get_bytes<KB>(slot + KB * (part + LPV * j));
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    x[8 * j + e] = cent[static_cast<uint32_t>(b >> (KB * e)) & ((1u << KB) - 1u)];
-                    nsq = fmaf(x[8 * j + e], x[8 * j + e], nsq);
-                }
-            }
-            nsq = sum_lanes<LPV>(nsq);
-            const float vec_norm = half_from_bits(*reinterpret_cast<const uint16_t*>(slot + S::kKeyIdxBytes));
-            float f = vec_norm * inv_sqrt_d;
-            if (p.nc) f = f / sqrtf(nsq);
-            fwht_local<EPL>(x);
-            fwht_lanes_fma<EPL, LPV>(x, part);
-            const uint4* msk = reinterpret_cast<const uint4*>(sign_mask[part]);
-#pragma unroll
-            for (int j = 0; j < EPL / 8; ++j) {
-                const uint4 m = msk[j];
-                const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) w[q] = bf16_pair(x[8 * j + 2 * q] * f, x[8 * j + 2 * q + 1] * f) ^ mw[q];
-                if (ok) kdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
+        dequant_vector<D, KB, VB>(slot, ok, kdst, vdst, part, cent, sign_mask[part], p.nc != 0, inv_sqrt_d);
+    }
+}
 
-        // ---- value ---------------------------------------------------------
-        {
-            const uint16_t* sz = reinterpret_cast<const uint16_t*>(slot + S::kKeyBytes + S::kValCodeBytes);
-            const float sc = half_from_bits(sz[0]);
-            const float z = half_from_bits(sz[1]);
-#pragma unroll
-            for (int j = 0; j < EPL / 8; ++j) {
-                const uint64_t b = get_bytes<VB>(slot + S::kKeyBytes + VB * (part + LPV * j));
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float c0 = static_cast<float>(static_cast<uint32_t>(b >> (VB * 2 * q)) & ((1u << VB) - 1u));
-                    const float c1 = static_cast<float>(static_cast<uint32_t>(b >> (VB * (2 * q + 1))) & ((1u << VB) - 1u));
-                    w[q] = bf16_pair(fmaf(sc, c0, z), fmaf(sc, c1, z));
-                }
-                if (ok) vdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+// Staged variant: each warp walks whole token steps (ts consecutive
+// positions of one block, ts * H * slot bytes, a multiple of 16 that starts
+// 16-byte aligned) and has a 2-slot ring in shared memory.  Lane 0 copies
+// the next step's rows with one bulk copy (cp.async.bulk, completing the
+// slot's mbarrier) while the warp expands the current one, so the slot
+// bytes come from shared memory instead of many small dependent global
+// loads.  The block-table entry of a step is read when its copy is issued,
+// one step ahead of its use.
+template <int D, int KB, int VB>
+__global__ void __launch_bounds__(kDqWarps * 32, 3)
+dequant_staged_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict__ block_table,
+                      const int max_blocks, const int32_t* __restrict__ cu_seqlens, const int max_seq_len,
+                      uint16_t* __restrict__ k_out, uint16_t* __restrict__ v_out, const FastDiv div_h,
+                      const FastDiv div_bs, const int ts, const int step_bytes) {
+    using S = Slot<D, KB, VB>;
+    using LS = LaneSplit<D>;
+    constexpr int EPL = LS::kEPL, LPV = LS::kLPV, VPW = LS::kVPW;
+    constexpr int SA = S::kAligned;
+    __shared__ float cent[16];
+    __shared__ __align__(16) uint32_t sign_mask[LPV][EPL / 2];
+    __shared__ __align__(8) uint64_t full[kDqWarps][2];
+    extern __shared__ __align__(16) uint8_t dq_ring[];  // [warp][slot][step_bytes]
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int part = lane % LPV;
+    const int vin = lane / LPV;
+    const int H = c.num_kv_heads;
+    const int s = blockIdx.y;
+    const int64_t row0 = cu_seqlens[s];
+    int n = cu_seqlens[s + 1] - cu_seqlens[s];
+    const int cap = min(max_seq_len, max_blocks * c.block_size);
+    if (n > cap || n < 0) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_flag(c.flags, kFlagSeq);
+        n = n < 0 ? 0 : cap;
+    }
+    if constexpr (KB != 8) {
+        if (threadIdx.x < 16) cent[threadIdx.x] = p.centroids[threadIdx.x < p.n_centroids ? threadIdx.x : 0];
+        for (int i = threadIdx.x; i < LPV * EPL / 2; i += kDqWarps * 32) {
+            const int pp = i / (EPL / 2), jw = i % (EPL / 2);
+            const int e = 8 * (pp + LPV * (jw / 4)) + 2 * (jw % 4);
+            const uint32_t b0 = (p.sign_mask[e / 32] >> (e % 32)) & 1u;
+            const uint32_t b1 = (p.sign_mask[(e + 1) / 32] >> ((e + 1) % 32)) & 1u;
+            sign_mask[pp][jw] = (b0 << 15) | (b1 << 31);
         }
+    }
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < kDqWarps; ++w) {
+            mbar_init(static_cast<uint32_t>(__cvta_generic_to_shared(&full[w][0])), 1u);
+            mbar_init(static_cast<uint32_t>(__cvta_generic_to_shared(&full[w][1])), 1u);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const float inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(D));
+
+    uint8_t* const ring = dq_ring + static_cast<int64_t>(warp) * 2 * step_bytes;
+    const uint32_t ring_sh = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    const uint32_t full_sh = static_cast<uint32_t>(__cvta_generic_to_shared(&full[warp][0]));
+    const int row_bytes = H * SA;
+    // lane 0: stage step kk (positions kk * ts ...) into slot sl; returns its block id (-1: none)
+    auto issue = [&](int kk, int sl) -> int {
+        const int pos = kk * ts;
+        const int col = static_cast<int>(fast_div(static_cast<uint32_t>(pos), div_bs));
+        const int b = block_table[static_cast<int64_t>(s) * max_blocks + col];
+        if (b >= 0 && b < c.num_blocks) {
+            const uint8_t* src = c.data + static_cast<int64_t>(b) * c.block_stride +
+                                 static_cast<int64_t>(pos - col * c.block_size) * row_bytes;
+            mbar_arrive_tx(full_sh + 8u * sl, static_cast<uint32_t>(step_bytes));
+            bulk_copy(ring_sh + static_cast<uint32_t>(sl * step_bytes), src, static_cast<uint32_t>(step_bytes),
+                      full_sh + 8u * sl);
+            return b;
+        }
+        mbar_arrive(full_sh + 8u * sl);
+        return -1;
+    };
+    const int steps_n = (n + ts - 1) / ts;
+    const int gstride = gridDim.x * kDqWarps;
+    int k = blockIdx.x * kDqWarps + warp;
+    int blk_cur = -1, blk_next = -1;
+    if (lane == 0 && k < steps_n) blk_cur = issue(k, 0);
+    bool timed_out = false;
+    int it = 0;
+    for (; k < steps_n; k += gstride, ++it) {
+        const int sl = it & 1;
+        __syncwarp();  // every lane is done with the other slot (the previous step)
+        if (lane == 0 && k + gstride < steps_n) {
+            fence_proxy_async();  // that slot was read through the generic proxy
+            blk_next = issue(k + gstride, sl ^ 1);
+        }
+        const int blk = __shfl_sync(kFull, blk_cur, 0);
+        if (!mbar_wait(full_sh + 8u * sl, static_cast<uint32_t>((it >> 1) & 1))) {
+            timed_out = true;
+            break;
+        }
+        const int pos0 = k * ts;
+        const uint8_t* stage = ring + sl * step_bytes;
+        for (int v0 = 0; v0 < ts * H; v0 += VPW) {
+            const int vl = v0 + vin;  // vector of the step: token vl / H, head vl % H
+            const int tl = static_cast<int>(fast_div(static_cast<uint32_t>(vl), div_h));
+            const int h = vl - tl * H;
+            const int pos = pos0 + tl;
+            const bool valid = vl < ts * H && pos < n;
+            const bool ok = valid && blk >= 0;
+            if (valid && blk < 0 && part == 0) set_flag(c.flags, kFlagBlock);
+            const uint8_t* slot = stage + (valid ? vl * SA : 0);
+            uint4* kdst = reinterpret_cast<uint4*>(k_out + ((row0 + pos) * H + h) * D) + part;
+            uint4* vdst = reinterpret_cast<uint4*>(v_out + ((row0 + pos) * H + h) * D) + part;
+            dequant_vector<D, KB, VB>(slot, ok, kdst, vdst, part, cent, sign_mask[part], p.nc != 0, inv_sqrt_d);
+        }
+        blk_cur = blk_next;
+    }
+    if (timed_out && lane == 0) {
+        set_flag(c.flags, kFlagWait);
+        // the other slot may still be filling: wait for it (bounded) before exiting
+        if (k + gstride < steps_n) mbar_wait(full_sh + 8u * ((it & 1) ^ 1), static_cast<uint32_t>(((it + 1) >> 1) & 1));
     }
 }
 
@@ -191,6 +322,43 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const int32_t* bt, 
                    const int32_t* cu, int num_seqs, int max_seq_len, uint16_t* k_out, uint16_t* v_out,
                    int sm_count, cudaStream_t stream) {
     constexpr int VPW = LaneSplit<D>::kVPW;
+    const FastDiv div_h = make_fast_div(static_cast<uint32_t>(c.num_kv_heads));
+    const FastDiv div_bs = make_fast_div(static_cast<uint32_t>(c.block_size));
+    // Staged kernel: token steps of ts rows whose bytes are a multiple of 16
+    // (ts = 16 / gcd(row, 16)) inside one block, a 16-byte aligned cache and
+    // block stride, and a ring that fits the shared memory.
+    {
+        const int64_t row = static_cast<int64_t>(c.num_kv_heads) * Slot<D, KB, VB>::kAligned;
+        int64_t g = row, m = 16;
+        while (m != 0) {
+            const int64_t r = g % m;
+            g = m;
+            m = r;
+        }
+        const int ts = static_cast<int>(16 / g);
+        const int64_t step_bytes = ts * row;
+        const size_t ring = static_cast<size_t>(kDqWarps) * 2 * static_cast<size_t>(step_bytes);
+        if (c.block_size % ts == 0 && c.block_stride % 16 == 0 && reinterpret_cast<uintptr_t>(c.data) % 16 == 0 &&
+            ring <= 160 * 1024) {
+            auto fn = dequant_staged_kernel<D, KB, VB>;
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(ring));
+            if (e != cudaSuccess) return e;
+            // about two waves of 4 CTAs per SM over all sequences, at most one
+            // step per warp per CTA column
+            const int64_t steps = (static_cast<int64_t>(max_seq_len) + ts - 1) / ts;
+            const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
+            int64_t gx = (target + num_seqs - 1) / (num_seqs > 0 ? num_seqs : 1);
+            const int64_t most = (steps + kDqWarps - 1) / kDqWarps;
+            if (gx > most) gx = most;
+            if (gx > 65535) gx = 65535;
+            if (gx < 1) gx = 1;
+            dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(num_seqs));
+            fn<<<grid, kDqWarps * 32, ring, stream>>>(p, c, bt, max_blocks, cu, max_seq_len, k_out, v_out, div_h,
+                                                      div_bs, ts, static_cast<int>(step_bytes));
+            return cudaGetLastError();
+        }
+    }
     const int64_t vecs = static_cast<int64_t>(max_seq_len) * c.num_kv_heads;
     int64_t gx = (vecs + VPW * kDqWarps - 1) / (VPW * kDqWarps);
     const int64_t wave_blocks = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * kDqBlocksPerSm * kDqMinWaves;
@@ -201,8 +369,6 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const int32_t* bt, 
     if (gx > 1024) gx = 1024;
     if (gx < 1) gx = 1;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(num_seqs));
-    const FastDiv div_h = make_fast_div(static_cast<uint32_t>(c.num_kv_heads));
-    const FastDiv div_bs = make_fast_div(static_cast<uint32_t>(c.block_size));
     const int narrow = vecs < (int64_t{1} << 32) ? 1 : 0;
     dequant_kernel<D, KB, VB><<<grid, kDqWarps * 32, 0, stream>>>(p, c, bt, max_blocks, cu, max_seq_len,
                                                                    k_out, v_out, div_h, div_bs, narrow);
