@@ -640,12 +640,23 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 
     // ---- value codes and (scale, zero) of one staged chunk, kept in registers
     // until the chunk's P.V one step later ------------------------------------------
+    // 2-byte value units of two tokens share one register (token 2c or 2c + 8
+    // in the low half, 2c + 1 or 2c + 9 in the high half): half the registers
+    // a chunk's values take while they wait for its P.V.
+    constexpr bool kPackV = G::VUNITS && G::VUNIT == 2;
+    constexpr int kVR2 = kPackV ? 1 : G::VREGS;
     struct VRegs {
-        uint32_t w0[G::VREGS], w1[G::VREGS], w8[G::VREGS], w9[G::VREGS];  // k-columns 2c, 2c+1, 2c+8, 2c+9
+        uint32_t w0[G::VREGS], w1[kVR2], w8[G::VREGS], w9[kVR2];  // k-columns 2c, 2c+1, 2c+8, 2c+9
         uint32_t sz0, sz1;  // half2 (scale, zero) of rows r, r + 8
     };
     auto load_v = [&](const uint8_t* stage, VRegs& vr) {
-        if constexpr (G::VUNITS) {
+        if constexpr (kPackV) {
+#pragma unroll
+            for (int m = 0; m < G::VNU; ++m) {
+                vr.w0[m] = prmt(ld_unit<2>(stage + v_off0 + 16 * m), ld_unit<2>(stage + v_off1 + 16 * m), 0x5410u);
+                vr.w8[m] = prmt(ld_unit<2>(stage + v_off8 + 16 * m), ld_unit<2>(stage + v_off9 + 16 * m), 0x5410u);
+            }
+        } else if constexpr (G::VUNITS) {
 #pragma unroll
             for (int m = 0; m < G::VNU; ++m) {
                 vr.w0[m] = ld_unit<G::VUNIT>(stage + v_off0 + 8 * G::VUNIT * m);
@@ -747,16 +758,16 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 #pragma unroll
         for (int mt = 0; mt < G::MTILES; ++mt) {
             uint32_t vf[4];
-            if constexpr (G::VUNITS && G::VUNIT == 2) {
-                // local dims 2mt, 2mt + 1 share byte b of unit m.  The units
-                // are zero-extended 16-bit loads, so one PRMT gives both
-                // tokens' byte b with a zero byte above it: the odd dim enters
-                // as the whole byte (16 hi + lo) and the epilogue subtracts
-                // the even dim's sum (lo), which the same MMA produces.
+            if constexpr (kPackV) {
+                // local dims 2mt, 2mt + 1 share byte b of unit m.  One PRMT
+                // gives both tokens' byte b (bytes b and b + 2 of the packed
+                // pair) with a zero byte above each: the odd dim enters as the
+                // whole byte (16 hi + lo) and the epilogue subtracts the even
+                // dim's sum (lo), which the same MMA produces.
                 const int m = (2 * mt) / G::VDPU, b = ((2 * mt) % G::VDPU) / 2;
-                const uint32_t sel = b | (2 << 4) | ((b + 4) << 8) | (6 << 12);
-                const uint32_t win0 = prmt(vr.w0[m], vr.w1[m], sel);
-                const uint32_t win8 = prmt(vr.w8[m], vr.w9[m], sel);
+                const uint32_t sel = b | (4 << 4) | ((b + 2) << 8) | (4 << 12);
+                const uint32_t win0 = prmt(vr.w0[m], 0u, sel);
+                const uint32_t win8 = prmt(vr.w8[m], 0u, sel);
                 vf[0] = win0 & 0x000F000Fu;
                 vf[1] = win0;
                 vf[2] = win8 & 0x000F000Fu;

@@ -315,3 +315,34 @@ def test_decode_in_cuda_graph(cuda_device):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(graphed.cpu().numpy(), eager.cpu().numpy())
     assert cache.error_flags() == 0
+
+
+def test_decode_on_a_workspace_left_by_another_plan(cuda_device):
+    """One workspace, never zero-filled, serves decodes with different split
+    counts and batches in a row (each call writes every partial state it
+    reads); the results match decodes on fresh workspaces."""
+    wl = W.small("c4", [600, 31, 200], layers=(2,))
+    layer_idx = wl.layers[-1]
+    k, v = wl.kv()
+    layer = oracle_layer(wl, layer_idx)
+    ocache, _ = oracle_cache(wl, layer, k, v)
+    cfg = host_cfg(wl)
+    cache = upload_cache(ocache, cfg, layer_idx, cuda_device)
+    q = bf16(wl.q(), cuda_device)
+    table = torch.from_numpy(wl.layout()[0]).to(cuda_device)
+    lens = torch.from_numpy(wl.seq_lens.astype(np.int32)).to(cuda_device)
+    max_len = int(wl.seq_lens.max())
+    size = max(tq.tq_decode_workspace_size(cfg, 3, wl.num_q_heads, wl.num_kv_heads, wl.block_size, max_len, sp)
+               for sp in (1, 2, 5, 9))
+    shared = torch.full((size,), 0x5A, dtype=torch.uint8, device=cuda_device)  # not zero-filled
+    for n_seq, splits in ((3, 9), (3, 2), (1, 5), (3, 1), (2, 5)):
+        fresh = torch.zeros(size, dtype=torch.uint8, device=cuda_device)
+        want = torch.empty((n_seq, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=cuda_device)
+        got = torch.full_like(want, float("nan"))
+        tq.tq_decode_attention(cfg, q[:n_seq], cache, table[:n_seq], lens[:n_seq], max_len, want, fresh,
+                               num_splits=splits)
+        tq.tq_decode_attention(cfg, q[:n_seq], cache, table[:n_seq], lens[:n_seq], max_len, got, shared,
+                               num_splits=splits)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(got.cpu().numpy(), want.cpu().numpy())
+    assert cache.error_flags() == 0
