@@ -68,35 +68,53 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w) {
 // One (token, head) vector: this lane's EPL elements of the key and the value
 // read from `slot` (global or shared memory) and written as bf16 to kdst /
 // vdst (16-byte groups LPV apart) when `ok`.
+//
+// jx < EPL / 8 sets the order in which the lane visits its 8-element groups:
+// step j reads group j ^ jx.  Lanes of different vectors then read different
+// groups at the same time, which spreads the reads of neighbouring slots in
+// shared memory over more banks.  Values and FP8 keys are written to the
+// group they were read from.  MSE keys keep group j ^ jx in registers 8 j ..
+// 8 j + 7 through the Walsh-Hadamard transform: relabelling the inputs by
+// XOR with 8 jx multiplies output 8 j + e by (-1)^popcount(jx & j) and
+// changes nothing else (each butterfly adds or subtracts the same two
+// values, possibly in swapped order, and rounding is symmetric under
+// negation), so that sign joins the random-sign mask of output group j.
 template <int D, int KB, int VB>
 __device__ __forceinline__ void dequant_vector(const uint8_t* slot, bool ok, uint4* kdst, uint4* vdst, int part,
-                                               const float* cent, const uint32_t* sign_mask_part, bool nc,
+                                               int jx, const float* cent, const uint32_t* sign_mask_part, bool nc,
                                                float inv_sqrt_d) {
     using S = Slot<D, KB, VB>;
     using LS = LaneSplit<D>;
     constexpr int EPL = LS::kEPL, LPV = LS::kLPV;
+    constexpr int NG = EPL / 8;
+    static_assert(NG == 1 || NG == 2 || NG == 4, "8-element groups per lane");
     // ---- key -----------------------------------------------------------
     if constexpr (KB == 8) {
 #pragma unroll
-        for (int j = 0; j < EPL / 8; ++j) {
-            const uint64_t b = get_bytes<8>(slot + 8 * (part + LPV * j));
+        for (int j = 0; j < NG; ++j) {
+            const int g = j ^ jx;
+            const uint64_t b = get_bytes<8>(slot + 8 * (part + LPV * g));
             uint32_t w[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) w[q] = e4m3x2_to_bf16x2(static_cast<uint32_t>(b >> (16 * q)));
-            if (ok) kdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
+            if (ok) kdst[LPV * g] = make_uint4(w[0], w[1], w[2], w[3]);
         }
     } else {
         float x[EPL];
-        float nsq = 0.f;
+        float ng[NG];  // sum of squares of each group; added in an XOR-invariant order
 #pragma unroll
-        for (int j = 0; j < EPL / 8; ++j) {
-            const uint64_t b = get_bytes<KB>(slot + KB * (part + LPV * j));
+        for (int j = 0; j < NG; ++j) {
+            const uint64_t b = get_bytes<KB>(slot + KB * (part + LPV * (j ^ jx)));
+            ng[j] = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 x[8 * j + e] = cent[static_cast<uint32_t>(b >> (KB * e)) & ((1u << KB) - 1u)];
-                nsq = fmaf(x[8 * j + e], x[8 * j + e], nsq);
+                ng[j] = fmaf(x[8 * j + e], x[8 * j + e], ng[j]);
             }
         }
+        float nsq = ng[0];
+        if constexpr (NG == 2) nsq = ng[0] + ng[1];
+        if constexpr (NG == 4) nsq = (ng[0] + ng[1]) + (ng[2] + ng[3]);
         nsq = sum_lanes<LPV>(nsq);
         const float vec_norm = half_from_bits(*reinterpret_cast<const uint16_t*>(slot + S::kKeyIdxBytes));
         float f = vec_norm * inv_sqrt_d;
@@ -105,9 +123,10 @@ __device__ __forceinline__ void dequant_vector(const uint8_t* slot, bool ok, uin
         fwht_lanes_fma<EPL, LPV>(x, part);
         const uint4* msk = reinterpret_cast<const uint4*>(sign_mask_part);
 #pragma unroll
-        for (int j = 0; j < EPL / 8; ++j) {
+        for (int j = 0; j < NG; ++j) {
             const uint4 m = msk[j];
-            const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
+            const uint32_t flip = (__popc(jx & j) & 1) ? 0x80008000u : 0u;
+            const uint32_t mw[4] = {m.x ^ flip, m.y ^ flip, m.z ^ flip, m.w ^ flip};
             uint32_t w[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) w[q] = bf16_pair(x[8 * j + 2 * q] * f, x[8 * j + 2 * q + 1] * f) ^ mw[q];
@@ -121,8 +140,9 @@ __device__ __forceinline__ void dequant_vector(const uint8_t* slot, bool ok, uin
         const float sc = half_from_bits(sz[0]);
         const float z = half_from_bits(sz[1]);
 #pragma unroll
-        for (int j = 0; j < EPL / 8; ++j) {
-            const uint64_t b = get_bytes<VB>(slot + S::kKeyBytes + VB * (part + LPV * j));
+        for (int j = 0; j < NG; ++j) {
+            const int g = j ^ jx;
+            const uint64_t b = get_bytes<VB>(slot + S::kKeyBytes + VB * (part + LPV * g));
             uint32_t w[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -130,7 +150,7 @@ __device__ __forceinline__ void dequant_vector(const uint8_t* slot, bool ok, uin
                 const float c1 = static_cast<float>(static_cast<uint32_t>(b >> (VB * (2 * q + 1))) & ((1u << VB) - 1u));
                 w[q] = bf16_pair(fmaf(sc, c0, z), fmaf(sc, c1, z));
             }
-            if (ok) vdst[LPV * j] = make_uint4(w[0], w[1], w[2], w[3]);
+            if (ok) vdst[LPV * g] = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
 }
@@ -195,7 +215,7 @@ dequant_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict
         uint4* kdst = reinterpret_cast<uint4*>(k_out + ((row0 + pos) * H + h) * D) + part;
         uint4* vdst = reinterpret_cast<uint4*>(v_out + ((row0 + pos) * H + h) * D) + part;
 
-        dequant_vector<D, KB, VB>(slot, ok, kdst, vdst, part, cent, sign_mask[part], p.nc != 0, inv_sqrt_d);
+        dequant_vector<D, KB, VB>(slot, ok, kdst, vdst, part, 0, cent, sign_mask[part], p.nc != 0, inv_sqrt_d);
     }
 }
 
@@ -212,7 +232,7 @@ __global__ void __launch_bounds__(kDqWarps * 32, 3)
 dequant_staged_kernel(const LayerParams p, const CacheGeom c, const int32_t* __restrict__ block_table,
                       const int max_blocks, const int32_t* __restrict__ cu_seqlens, const int max_seq_len,
                       uint16_t* __restrict__ k_out, uint16_t* __restrict__ v_out, const FastDiv div_h,
-                      const FastDiv div_bs, const int ts, const int step_bytes) {
+                      const FastDiv div_bs, const int ts, const int step_bytes, const uint32_t order) {
     using S = Slot<D, KB, VB>;
     using LS = LaneSplit<D>;
     constexpr int EPL = LS::kEPL, LPV = LS::kLPV, VPW = LS::kVPW;
@@ -225,6 +245,11 @@ dequant_staged_kernel(const LayerParams p, const CacheGeom c, const int32_t* __r
     const int warp = threadIdx.x >> 5;
     const int part = lane % LPV;
     const int vin = lane / LPV;
+    // group order of this lane's vectors: j ^ jx, jx = (a vin + b (vin >> 2) + c (vin >> 3)) mod groups
+    // (d < 64: one vector per lane or one group, the natural order)
+    const int jx = D < 64 ? 0
+                          : static_cast<int>(((order & 3u) * vin + ((order >> 2) & 3u) * (vin >> 2) +
+                                              ((order >> 4) & 3u) * (vin >> 3)) % static_cast<uint32_t>(EPL / 8));
     const int H = c.num_kv_heads;
     const int s = blockIdx.y;
     const int64_t row0 = cu_seqlens[s];
@@ -306,7 +331,8 @@ dequant_staged_kernel(const LayerParams p, const CacheGeom c, const int32_t* __r
             const uint8_t* slot = stage + (valid ? vl * SA : 0);
             uint4* kdst = reinterpret_cast<uint4*>(k_out + ((row0 + pos) * H + h) * D) + part;
             uint4* vdst = reinterpret_cast<uint4*>(v_out + ((row0 + pos) * H + h) * D) + part;
-            dequant_vector<D, KB, VB>(slot, ok, kdst, vdst, part, cent, sign_mask[part], p.nc != 0, inv_sqrt_d);
+            dequant_vector<D, KB, VB>(slot, ok, kdst, vdst, part, jx, cent, sign_mask[part], p.nc != 0,
+                                      inv_sqrt_d);
         }
         blk_cur = blk_next;
     }
@@ -315,6 +341,73 @@ dequant_staged_kernel(const LayerParams p, const CacheGeom c, const int32_t* __r
         // the other slot may still be filling: wait for it (bounded) before exiting
         if (k + gstride < steps_n) mbar_wait(full_sh + 8u * ((it & 1) ^ 1), static_cast<uint32_t>(((it + 1) >> 1) & 1));
     }
+}
+
+// Shared-memory wavefronts of the staged kernel's slot reads under one group
+// order (see dequant_vector): for 8 consecutive warp steps over a staged
+// run of slots, each load instruction costs the largest number of distinct
+// 4-byte words that one of the 32 banks has to serve.
+template <int D, int KB, int VB>
+long slot_read_wavefronts(uint32_t order) {
+    using S = Slot<D, KB, VB>;
+    using LS = LaneSplit<D>;
+    constexpr int EPL = LS::kEPL, LPV = LS::kLPV, VPW = LS::kVPW, NG = EPL / 8;
+    // one entry per load instruction of a lane: (field start, bytes per group, byte in the group)
+    struct Load {
+        int base, unit, off;
+        bool per_group;
+    };
+    Load loads[2 * NG * 4 + 3];
+    int nl = 0;
+    const int kstep = KB == 8 ? 2 : (KB == 4 ? 2 : 1), kn = KB == 8 ? 4 : (KB == 4 ? 2 : 3);
+    for (int i = 0; i < kn; ++i) loads[nl++] = {0, KB, i * kstep, true};
+    if (KB != 8) loads[nl++] = {S::kKeyIdxBytes, 0, 0, false};
+    const int vstep = VB == 4 ? 2 : 1, vn = VB == 4 ? 2 : 3;
+    for (int i = 0; i < vn; ++i) loads[nl++] = {S::kKeyBytes, VB, i * vstep, true};
+    loads[nl++] = {S::kKeyBytes + S::kValCodeBytes, 0, 0, false};
+    loads[nl++] = {S::kKeyBytes + S::kValCodeBytes + 2, 0, 0, false};
+    long total = 0;
+    for (int st = 0; st < 8; ++st) {
+        for (int li = 0; li < nl; ++li) {
+            const Load& ld = loads[li];
+            for (int j = 0; j < (ld.per_group ? NG : 1); ++j) {
+                long words[32];
+                int bank_n[32] = {0};
+                for (int lane = 0; lane < 32; ++lane) {
+                    const int vin = lane / LPV, part = lane % LPV;
+                    const int jx = static_cast<int>(((order & 3u) * vin + ((order >> 2) & 3u) * (vin >> 2) +
+                                                     ((order >> 4) & 3u) * (vin >> 3)) % NG);
+                    const long addr = static_cast<long>(st * VPW + vin) * S::kAligned + ld.base +
+                                      (ld.per_group ? ld.unit * (part + LPV * (j ^ jx)) + ld.off : 0);
+                    words[lane] = addr / 4;
+                    bool seen = false;
+                    for (int o = 0; o < lane && !seen; ++o) seen = words[o] == words[lane];
+                    if (!seen) ++bank_n[words[lane] % 32];
+                }
+                int most = 0;
+                for (int bk = 0; bk < 32; ++bk) most = bank_n[bk] > most ? bank_n[bk] : most;
+                total += most;
+            }
+        }
+    }
+    return total;
+}
+
+// The group order with the fewest wavefronts among jx = (a vin + b (vin >> 2)
+// + c (vin >> 3)) mod groups, packed as a | b << 2 | c << 4 (0: the natural order).
+template <int D, int KB, int VB>
+uint32_t best_group_order() {
+    if (D < 64) return 0u;
+    uint32_t best = 0u;
+    long best_w = slot_read_wavefronts<D, KB, VB>(0u);
+    for (uint32_t code = 1; code < 64; ++code) {
+        const long w = slot_read_wavefronts<D, KB, VB>(code);
+        if (w < best_w) {
+            best_w = w;
+            best = code;
+        }
+    }
+    return best;
 }
 
 template <int D, int KB, int VB>
@@ -354,8 +447,9 @@ cudaError_t launch(const LayerParams& p, const CacheGeom& c, const int32_t* bt, 
             if (gx > 65535) gx = 65535;
             if (gx < 1) gx = 1;
             dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(num_seqs));
+            static const uint32_t order = best_group_order<D, KB, VB>();
             fn<<<grid, kDqWarps * 32, ring, stream>>>(p, c, bt, max_blocks, cu, max_seq_len, k_out, v_out, div_h,
-                                                      div_bs, ts, static_cast<int>(step_bytes));
+                                                      div_bs, ts, static_cast<int>(step_bytes), order);
             return cudaGetLastError();
         }
     }
