@@ -10,6 +10,8 @@ so the GPU decodes oracle bytes there.  The GPU then decodes the full batch,
 and the rows of those query heads are compared with the oracle's decode
 within the decode tolerance.  No oracle input comes from the CUDA path.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -79,19 +81,18 @@ DEQUANT_SAMPLES = {"c3": 2, "c4": 6, "c2": 2}
 
 def _dequant_steps(wl):
     """Grid-stride ranges of the dequant's full-size launch, as positions:
-    (steps per warp, positions one step covers).  Mirrors the launch's
-    arithmetic in tq_dequant.cu (8 warps, 4 resident blocks per SM over at
-    least 4 waves, at most 4 steps with MSE keys, at most 1024 blocks per
-    sequence) for a 152-SM GB300."""
-    vpw = 32 // max(1, wl.head_dim // 32)  # vectors per warp: 32 / (d / min(d, 32))
-    vecs = int(wl.seq_lens.max()) * wl.num_kv_heads
-    gx = -(-vecs // (vpw * 8))
+    (steps per warp, positions one step of the grid covers).  Mirrors the
+    staged launch in tq_dequant.cu: token steps of ts = 16 / gcd(H * slot, 16)
+    positions, 8 warps per block, about 8 blocks per SM across all sequences,
+    at most one step per warp per block column."""
+    cfg = host_cfg(wl)
+    ts = 16 // math.gcd(wl.num_kv_heads * cfg.slot_size_aligned, 16)
+    steps_n = -(-int(wl.seq_lens.max()) // ts)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    iters = gx * wl.num_seqs // (sms * 4 * 4)
-    iters = max(1, min(1 if wl.key_bits == 8 else 4, iters))
-    gx = min(1024, max(1, -(-gx // iters)))
-    per_step = gx * 8 * vpw // wl.num_kv_heads
-    steps = -(-vecs // (gx * 8 * vpw))
+    gx = -(-sms * 8 // wl.num_seqs)
+    gx = max(1, min(gx, -(-steps_n // 8), 65535))
+    per_step = gx * 8 * ts
+    steps = -(-steps_n // (gx * 8))
     return steps, per_step
 
 

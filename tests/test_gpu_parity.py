@@ -139,6 +139,38 @@ def test_dequant_parity(cuda_device, wl):
     assert np.all(np.abs(kg - kw) <= tol)
 
 
+@pytest.mark.parametrize("wl", [c for c in CASES if c.head_dim >= 64], ids=[i for c, i in zip(CASES, IDS)
+                                                                      if c.head_dim >= 64])
+def test_dequant_parity_16_byte_aligned_outputs(cuda_device, wl):
+    """Outputs that start 16 bytes past a 32-byte boundary (the least
+    alignment tq_dequant accepts): every 16-byte group store lands in place
+    and nothing is written before the first row."""
+    layer_idx = wl.layers[-1]
+    k, v = wl.kv()
+    layer = oracle_layer(wl, layer_idx)
+    ocache, _ = oracle_cache(wl, layer, k, v)
+    cfg = host_cfg(wl)
+    cache = upload_cache(ocache, cfg, layer_idx, cuda_device)
+    table = wl.layout()[0]
+    cu = wl.cu_seqlens()
+    rows = int(cu[-1])
+    n = rows * wl.num_kv_heads * wl.head_dim
+    kbuf = torch.full((n + 8,), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+    vbuf = torch.full_like(kbuf, float("nan"))
+    assert kbuf.data_ptr() % 32 == 0
+    k_out = kbuf[8:].view(rows, wl.num_kv_heads, wl.head_dim)  # 16 bytes past the boundary
+    v_out = vbuf[8:].view(rows, wl.num_kv_heads, wl.head_dim)
+    tq.tq_dequant(cfg, cache, torch.from_numpy(table).to(cuda_device), torch.from_numpy(cu).to(cuda_device),
+                  int(wl.seq_lens.max()), k_out, v_out)
+    torch.cuda.synchronize()
+    kw, vw = O.dequant_cache(layer, ocache, table, cu)
+    np.testing.assert_array_equal(v_out.float().cpu().numpy(), vw)
+    kg = k_out.float().cpu().numpy()
+    tol = np.abs(kw) * 2.0 ** -7 + 1e-6 * np.abs(kw).max(axis=-1, keepdims=True)
+    assert np.all(np.abs(kg - kw) <= tol)
+    assert torch.isnan(kbuf[:8].float()).all() and torch.isnan(vbuf[:8].float()).all()  # nothing before the rows
+
+
 def test_fp8_keys_exhaustive_bf16(cuda_device):
     """All finite bf16 bit patterns as FP8 keys (d=128, 512 vectors)."""
     pat = np.arange(65536, dtype=np.uint32)
