@@ -76,13 +76,23 @@ __device__ __forceinline__ void put_bytes(uint8_t* dst, uint64_t bits, bool two_
     }
 }
 
-// Packs 8 codes of B bits LSB-first.
+// Packs 8 codes of B bits LSB-first (B <= 4: one 32-bit word).
 template <int B>
 __device__ __forceinline__ uint64_t pack8(const uint32_t* code) {
-    uint64_t w = 0;
+    if constexpr (B <= 4) {
+        uint32_t lo = 0, hi = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) w |= static_cast<uint64_t>(code[e]) << (B * e);
-    return w;
+        for (int e = 0; e < 4; ++e) {
+            lo |= code[e] << (B * e);
+            hi |= code[4 + e] << (B * e);
+        }
+        return static_cast<uint64_t>(lo | (hi << (4 * B)));
+    } else {
+        uint64_t w = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w |= static_cast<uint64_t>(code[e]) << (B * e);
+        return w;
+    }
 }
 
 // Token map of a ring append ([ART] hnwysp.cn article, "full_tq
