@@ -398,13 +398,22 @@ long slot_read_wavefronts(uint32_t order) {
 template <int D, int KB, int VB>
 uint32_t best_group_order() {
     if (D < 64) return 0u;
+    // b matters only with more than 4 vectors per warp, c with more than 8
+    constexpr int VPW = LaneSplit<D>::kVPW;
+    const uint32_t nb = VPW > 4 ? 4u : 1u, nc = VPW > 8 ? 4u : 1u;
     uint32_t best = 0u;
     long best_w = slot_read_wavefronts<D, KB, VB>(0u);
-    for (uint32_t code = 1; code < 64; ++code) {
-        const long w = slot_read_wavefronts<D, KB, VB>(code);
-        if (w < best_w) {
-            best_w = w;
-            best = code;
+    for (uint32_t c = 0; c < nc; ++c) {
+        for (uint32_t b = 0; b < nb; ++b) {
+            for (uint32_t a = 0; a < 4; ++a) {
+                const uint32_t code = a | (b << 2) | (c << 4);
+                if (code == 0u) continue;
+                const long w = slot_read_wavefronts<D, KB, VB>(code);
+                if (w < best_w) {
+                    best_w = w;
+                    best = code;
+                }
+            }
         }
     }
     return best;
