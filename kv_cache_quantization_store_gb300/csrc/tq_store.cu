@@ -388,19 +388,28 @@ store_kernel(const LayerParams p, const CacheGeom c, const uint16_t* __restrict_
         // ---- value ---------------------------------------------------------
         {
             float2 x2[EPL / 2];
+            // min and max on the bf16 pairs (packed min/max, the same choices
+            // as on the fp32 values: NaN loses to a number, -0 below +0)
+            __nv_bfloat162 mn2, mx2;
 #pragma unroll
             for (int j = 0; j < EPL / 8; ++j) {
                 const uint4 u = ld16(vsrc, j);
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) x2[4 * j + q] = make_float2(bf16_lo(w[q]), bf16_hi(w[q]));
+                for (int q = 0; q < 4; ++q) {
+                    x2[4 * j + q] = make_float2(bf16_lo(w[q]), bf16_hi(w[q]));
+                    const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[q]);
+                    if (j == 0 && q == 0) {
+                        mn2 = b2;
+                        mx2 = b2;
+                    } else {
+                        mn2 = __hmin2(mn2, b2);
+                        mx2 = __hmax2(mx2, b2);
+                    }
+                }
             }
-            float mn = fminf(x2[0].x, x2[0].y), mx = fmaxf(x2[0].x, x2[0].y);
-#pragma unroll
-            for (int i = 1; i < EPL / 2; ++i) {
-                mn = fminf(mn, fminf(x2[i].x, x2[i].y));
-                mx = fmaxf(mx, fmaxf(x2[i].x, x2[i].y));
-            }
+            float mn = fminf(__low2float(mn2), __high2float(mn2));
+            float mx = fmaxf(__low2float(mx2), __high2float(mx2));
             mn = min_lanes<LPV>(mn);
             mx = max_lanes<LPV>(mx);
             const uint16_t sb = half_bits(__fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(kTopV)));
