@@ -232,6 +232,10 @@ struct Geo {
     static constexpr int LUT_REP = LREP;                    // copies of the table (lanes l and l + LREP share one)
     static constexpr int LUT_SHIFT = LREP == 32 ? 7 : 6;    // log2 of an entry's stride (LREP x 4 bytes)
     static constexpr int LUT_BYTES = LUT_ENTRIES * LREP * 4;  // half2 per entry and copy
+    // 4-bit keys of packed-query kernels at 3 CTAs per SM (the 16-copy table):
+    // key codes held as 32-bit words of two k-steps, read as 4-byte units by
+    // warps whose share is 4-byte aligned
+    static constexpr bool PAIR_K = KB == 4 && PACKQ && LREP == 16 && KSTEPS % 2 == 0;
     static constexpr int XCH_W = WPH > 1 ? 32 * 6 * 4 : 0;  // per warp and buffer: 32 x {4 scores, 2 norms}
     static constexpr int X_OFF = LUT_BYTES;
     // control block: full mbarrier, release counter, block id per stage; error word
@@ -371,11 +375,22 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
         }
     }
 
+    // 4-bit keys: a warp whose share of every token's key codes starts on a
+    // 4-byte boundary reads 4-byte units (two k-steps each, lane c taking
+    // units c + 4m), the others 2-byte units (one k-step, units c + 4j) that
+    // it pairs into the same 32-bit form.
+    const int hs = h * SA;
+    constexpr bool kPairK = G::PAIR_K;
+    const bool ku4 = kPairK && ROW % 4 == 0 && (hs + part * G::KSH) % 4 == 0;
     // First of the 4 consecutive key dims lane c of warp part covers at local
     // k-step jl (the lane layout of the key loads).
-    auto key_dim0 = [](int c_, int part_, int jl) -> int {
-        if constexpr (G::KUNITS) return part_ * (D / WPH) + 4 * (c_ + 4 * jl);
-        else return c_ * (D / 4) + part_ * (D / (4 * WPH)) + 4 * jl;
+    auto key_dim0 = [&](int c_, int part_, int jl) -> int {
+        if constexpr (G::KUNITS) {
+            if (kPairK && ku4) return part_ * (D / WPH) + 8 * (c_ + 4 * (jl / 2)) + 4 * (jl % 2);
+            return part_ * (D / WPH) + 4 * (c_ + 4 * jl);
+        } else {
+            return c_ * (D / 4) + part_ * (D / (4 * WPH)) + 4 * jl;
+        }
     };
 
     // ---- queries: q' = Pi q (MSE keys), scaled, into B fragments ---------------
@@ -492,8 +507,8 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
     // spread each warp's loads over the shared-memory banks. -------------------
     auto sig = [&](int k) -> int { return a.tok_eo ? (k < 8 ? 2 * k : 2 * (k - 8) + 1) : k; };
     const int tq0 = sig(r), tq1 = sig(r + 8);  // QK rows r, r + 8
-    const int hs = h * SA;
-    const int kbase = G::KUNITS ? hs + part * G::KSH + G::KUNIT * cc : hs + cc * G::KBYTES + part * G::KBYTES_W;
+    const int kbase = G::KUNITS ? hs + part * G::KSH + (ku4 ? 4 : G::KUNIT) * cc
+                                : hs + cc * G::KBYTES + part * G::KBYTES_W;
     const int k_off0 = tq0 * ROW + kbase, k_off1 = tq1 * ROW + kbase;
     const int n_off0 = tq0 * ROW + hs + S::kKeyIdxBytes, n_off1 = tq1 * ROW + hs + S::kKeyIdxBytes;
     const int z_off0 = tq0 * ROW + hs + S::kKeyBytes + S::kValCodeBytes;
@@ -516,9 +531,24 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) qacc[i][e] = 0.f;
         float nacc[4] = {0.f, 0.f, 0.f, 0.f};
-        constexpr int KREGS = G::KUNITS ? G::KSTEPS : G::KWORDS;
+        constexpr int KREGS = kPairK ? G::KSTEPS / 2 : (G::KUNITS ? G::KSTEPS : G::KWORDS);
         uint32_t kw0[KREGS], kw1[KREGS];
-        if constexpr (G::KUNITS) {
+        if constexpr (kPairK) {
+            // word m: k-step 2m in the low half, 2m + 1 in the high half
+            if (ku4) {
+#pragma unroll
+                for (int m = 0; m < KREGS; ++m) {
+                    kw0[m] = ld32(stage + k_off0 + 16 * m);
+                    kw1[m] = ld32(stage + k_off1 + 16 * m);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < KREGS; ++m) {
+                    kw0[m] = prmt(ld_unit<2>(stage + k_off0 + 16 * m), ld_unit<2>(stage + k_off0 + 16 * m + 8), 0x5410u);
+                    kw1[m] = prmt(ld_unit<2>(stage + k_off1 + 16 * m), ld_unit<2>(stage + k_off1 + 16 * m + 8), 0x5410u);
+                }
+            }
+        } else if constexpr (G::KUNITS) {
 #pragma unroll
             for (int m = 0; m < KREGS; ++m) {
                 kw0[m] = ld_unit<G::KUNIT>(stage + k_off0 + 4 * G::KUNIT * m);
@@ -537,8 +567,23 @@ decode_kernel(const LayerParams p, const CacheGeom c, const Args a) {
                 // unit j: 4 FP8 codes; each 16-bit half is one e4m3 pair -> f16x2
                 e4m3x4_to_f16x2(kw0[j], af[0], af[2]);
                 e4m3x4_to_f16x2(kw1[j], af[1], af[3]);
+            } else if constexpr (kPairK) {
+                // k-step j: two pair codes, bytes 2 (j % 2) and 2 (j % 2) + 1 of
+                // word j / 2, moved to the table's entry stride
+                constexpr int kS = G::LUT_SHIFT;
+                constexpr uint32_t kM = 0xFFu << kS;
+                const uint32_t w0 = kw0[j >> 1], w1 = kw1[j >> 1];
+                const bool hi = (j & 1) != 0;  // a constant once the loop is unrolled
+                const uint32_t p0 = hi ? (w0 >> (16 - kS)) : (w0 << kS);
+                const uint32_t p1 = hi ? (w1 >> (16 - kS)) : (w1 << kS);
+                const uint32_t q0 = hi ? (w0 >> (24 - kS)) : (w0 >> (8 - kS));
+                const uint32_t q1 = hi ? (w1 >> (24 - kS)) : (w1 >> (8 - kS));
+                af[0] = ld32(lut + ((p0 & kM) | lane4));
+                af[1] = ld32(lut + ((p1 & kM) | lane4));
+                af[2] = ld32(lut + ((q0 & kM) | lane4));
+                af[3] = ld32(lut + ((q1 & kM) | lane4));
             } else if constexpr (KB == 4) {
-                // unit j: two pair codes, one per byte, moved to bit 7 (table rows of 128 bytes)
+                // unit j: two pair codes, one per byte, moved to the table's entry stride
                 constexpr int kS = G::LUT_SHIFT;
                 constexpr uint32_t kM = 0xFFu << kS;
                 af[0] = ld32(lut + (((kw0[j] << kS) & kM) | lane4));
@@ -996,15 +1041,17 @@ int load_wavefronts(bool eo) {
         const int hs = h * G::SA;
         for (int part = 0; part < WPH; ++part) {
             for (int k = 0; k < 16; k += 8) {
+                const bool u4 = G::PAIR_K && G::ROW % 4 == 0 && (hs + part * G::KSH) % 4 == 0;
                 for (int l = 0; l < 32; ++l) {
                     const int r = l / 4, c = l % 4;
-                    const int base = G::KUNITS ? hs + part * G::KSH + G::KUNIT * c
+                    const int base = G::KUNITS ? hs + part * G::KSH + (u4 ? 4 : G::KUNIT) * c
                                                : hs + c * G::KBYTES + part * G::KBYTES_W;
                     addr[l] = sig(r + k) * G::ROW + base;
                     if (!G::KUNITS) addr[l] &= ~3;
                 }
-                total += G::KUNITS ? bank_wavefronts(addr, G::KUNIT) * G::KSTEPS
-                                   : bank_wavefronts(addr, 4) * (G::KWORDS + 1);
+                total += !G::KUNITS ? bank_wavefronts(addr, 4) * (G::KWORDS + 1)
+                                    : (u4 ? bank_wavefronts(addr, 4) * (G::KSTEPS / 2)
+                                          : bank_wavefronts(addr, G::KUNIT) * G::KSTEPS);
             }
             const int kcols[4] = {0, 1, 8, 9};
             for (int kc : kcols) {
