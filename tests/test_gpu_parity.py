@@ -36,6 +36,11 @@ def small_cases():
         W.custom(256, 8, 4, False, 2, 16, 48, [200], 2005),
         W.custom(256, 3, 3, True, 1, 1, 16, [77], 2006, kv_mode="outliers"),
         W.custom(128, 4, 4, False, 8, 64, 64, [300, 129], 2007),
+        # 4-bit keys in the paired-word decode: every warp's key share
+        # 2 bytes off a word (H = 1), and even / odd heads mixed (H = 2, 4)
+        W.custom(256, 4, 4, True, 1, 4, 16, [300, 17], 2011),
+        W.custom(256, 4, 4, True, 2, 4, 32, [129, 64], 2012),
+        W.custom(128, 4, 4, True, 4, 16, 16, [97, 250], 2013),
     ]
 
 
